@@ -1,0 +1,146 @@
+"""GB300 (sm_103a) causal attention forward: FP8 e4m3 with Lean P / exact P,
+per-64-key power-of-two block scaling and division by the sum of the rounded
+probabilities, and the BF16 path beside it.
+
+This module is the thin Python binding of ``libzyfa.so`` (C ABI declared in
+``include/zyfa.h``).  It only marshals arguments: every step of the
+computation runs in the library's CUDA kernels.  PyTorch is used for device
+memory and streams.  There is no CPU fallback: when the library has not been
+built, importing the binding's functions raises.
+
+Method: "ZYFA: Speed and Accuracy of FP8 FlashAttention on AMD CDNA4"
+(Sec. II-B, II-C, IV-A, IV-B).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB_PATH, build  # noqa: F401
+
+ZYFA_OK = 0
+ZYFA_ERR_NULL = -1
+ZYFA_ERR_SHAPE = -2
+ZYFA_ERR_UNSUPPORTED = -3
+ZYFA_ERR_ALIGN = -4
+ZYFA_ERR_CUDA = -5
+ZYFA_ERR_TIMEOUT = -6
+ZYFA_P_EXACT = 0
+ZYFA_P_LEAN = 1
+
+EXPORTS = ("zyfa_fwd", "zyfa_fwd_bf16", "zyfa_status_string",
+           "zyfa_last_device_status", "zyfa_version")
+
+_lib = None
+
+
+class ZyfaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {zyfa_status_string(status)} (status {status})")
+
+
+def load():
+    """Load libzyfa.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: the CUDA library must be built first "
+            "(fp8_causal_flashattention_gb300.build() or __graft_entry__.build())")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, ci = ctypes.c_void_p, ctypes.c_int
+    lib.zyfa_fwd.restype = ci
+    lib.zyfa_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp] + [ci] * 9 + [vp]
+    lib.zyfa_fwd_bf16.restype = ci
+    lib.zyfa_fwd_bf16.argtypes = [vp, vp, vp, vp] + [ci] * 7 + [vp]
+    lib.zyfa_status_string.restype = ctypes.c_char_p
+    lib.zyfa_status_string.argtypes = [ci]
+    lib.zyfa_last_device_status.restype = ci
+    lib.zyfa_last_device_status.argtypes = [vp]
+    lib.zyfa_version.restype = ci
+    lib.zyfa_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _ptr(x):
+    """Device address of a tensor (or an int / None passed through)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ---------------------------------------------------------------- C ABI, 1:1
+def zyfa_fwd(q, k, v, descale_q, descale_k, descale_v, out, B, Hq, Hkv, N, d_qk, d_v,
+             causal=1, p_mode=ZYFA_P_LEAN, block_scale=1, stream=None) -> int:
+    """``zyfa_fwd`` of include/zyfa.h; tensors or raw device addresses."""
+    return load().zyfa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(descale_q), _ptr(descale_k),
+                           _ptr(descale_v), _ptr(out), B, Hq, Hkv, N, d_qk, d_v, causal,
+                           p_mode, block_scale, _stream(stream))
+
+
+def zyfa_fwd_bf16(q, k, v, out, B, Hq, Hkv, N, d_qk, d_v, causal=1, stream=None) -> int:
+    """``zyfa_fwd_bf16`` of include/zyfa.h; tensors or raw device addresses."""
+    return load().zyfa_fwd_bf16(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, N, d_qk,
+                                d_v, causal, _stream(stream))
+
+
+def zyfa_status_string(status: int) -> str:
+    return load().zyfa_status_string(int(status)).decode()
+
+
+def zyfa_last_device_status(stream=None) -> int:
+    return load().zyfa_last_device_status(_stream(stream))
+
+
+def zyfa_version() -> int:
+    return load().zyfa_version()
+
+
+# ---------------------------------------------------------------- conveniences
+def _shape(q, k, v):
+    B, N, Hq, d_qk = q.shape
+    if k.shape[0] != B or k.shape[1] != N or v.shape[:3] != k.shape[:3] or k.shape[3] != d_qk:
+        raise ValueError("q, k, v must be BSHD with matching B, N, Hkv and d_qk")
+    return B, N, Hq, k.shape[2], d_qk, v.shape[3]
+
+
+def attention_fp8(q, k, v, descale_q=None, descale_k=None, descale_v=None, *,
+                  p_mode=ZYFA_P_LEAN, block_scale=1, out=None, stream=None):
+    """Causal FP8 attention on e4m3 tensors (torch.float8_e4m3fn or uint8),
+    BSHD; descales are 1-element float32 device tensors (or None for 1.0).
+    Returns the BF16 output [B, N, Hq, d_v]."""
+    import torch
+    B, N, Hq, Hkv, d_qk, d_v = _shape(q, k, v)
+    if out is None:
+        out = torch.empty((B, N, Hq, d_v), dtype=torch.bfloat16, device=q.device)
+    rc = zyfa_fwd(q, k, v, descale_q, descale_k, descale_v, out, B, Hq, Hkv, N, d_qk, d_v,
+                  1, p_mode, block_scale, stream)
+    if rc != ZYFA_OK:
+        raise ZyfaError(rc, "zyfa_fwd")
+    return out
+
+
+def attention_bf16(q, k, v, *, out=None, stream=None):
+    """Causal BF16 attention, BSHD.  Returns the BF16 output."""
+    import torch
+    B, N, Hq, Hkv, d_qk, d_v = _shape(q, k, v)
+    if out is None:
+        out = torch.empty((B, N, Hq, d_v), dtype=torch.bfloat16, device=q.device)
+    rc = zyfa_fwd_bf16(q, k, v, out, B, Hq, Hkv, N, d_qk, d_v, 1, stream)
+    if rc != ZYFA_OK:
+        raise ZyfaError(rc, "zyfa_fwd_bf16")
+    return out

@@ -1,0 +1,153 @@
+// zyfa_api.cu -- C ABI entry points (include/zyfa.h): argument checks,
+// TMA tensor-map encoding and kernel launch on the caller's stream.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/zyfa.h"
+#include "fwd.cuh"
+
+namespace zyfa {
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 4-D map over a BSHD tensor: dims (d, H, N, B), box (inner, 1, 128, 1).
+bool make_map(CUtensorMap* m, const void* base, bool bf16, int d, int H, int N, int B,
+              int box_inner, CUtensorMapSwizzle swz) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const uint64_t esz = bf16 ? 2 : 1;
+    cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                          static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
+    cuuint64_t strides[3] = {d * esz, static_cast<uint64_t>(H) * d * esz,
+                             static_cast<uint64_t>(N) * H * d * esz};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(box_inner), 1, 128, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
+                     const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_common(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
+                 int N, int d_qk, int d_v, int causal, int esz) {
+    if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0) return ZYFA_ERR_SHAPE;
+    if (causal != 1) return ZYFA_ERR_UNSUPPORTED;
+    if (!((d_qk == 128 || d_qk == 192) && d_v == 128)) return ZYFA_ERR_UNSUPPORTED;
+    if (Hq % Hkv != 0) return ZYFA_ERR_SHAPE;
+    if (N % 128 != 0) return ZYFA_ERR_SHAPE;
+    if (B == 0 || N == 0) return ZYFA_OK;
+    if (!q || !k || !v || !out) return ZYFA_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+        return ZYFA_ERR_ALIGN;
+    // TMA limits: global dims < 2^32, byte strides < 2^40; grid < 2^31
+    const uint64_t bstride = static_cast<uint64_t>(N) * Hq * d_qk * esz;
+    if (bstride >= (1ull << 40)) return ZYFA_ERR_SHAPE;
+    if (static_cast<uint64_t>(B) * Hq * (N / 128) >= (1ull << 31)) return ZYFA_ERR_SHAPE;
+    return 1;   // proceed
+}
+
+template <bool FP8, int DQK>
+int launch(const void* q, const void* k, const void* v, const FwdArgs& a, cudaStream_t stream) {
+    using C = FwdCfg<FP8, DQK>;
+    CUtensorMap tq, tk, tv;
+    const CUtensorMapSwizzle swz =
+        C::CB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const int inner = C::CB / C::ESZ;
+    if (!make_map(&tq, q, !FP8, DQK, a.Hq, a.N, a.B, inner, swz)) return ZYFA_ERR_CUDA;
+    if (!make_map(&tk, k, !FP8, DQK, a.Hkv, a.N, a.B, inner, swz)) return ZYFA_ERR_CUDA;
+    if (!make_map(&tv, v, !FP8, C::DV, a.Hkv, a.N, a.B, 128 / C::ESZ, CU_TENSOR_MAP_SWIZZLE_128B))
+        return ZYFA_ERR_CUDA;
+    auto kern = zyfa_fwd_kernel<FP8, DQK>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
+        cudaSuccess)
+        return ZYFA_ERR_CUDA;
+    const unsigned grid = static_cast<unsigned>(a.B) * a.Hq * (a.N / C::BM);
+    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, a);
+    return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace zyfa
+
+using namespace zyfa;
+
+extern "C" int zyfa_fwd(const void* q, const void* k, const void* v, const float* descale_q,
+                        const float* descale_k, const float* descale_v, void* out, int B, int Hq,
+                        int Hkv, int N, int d_qk, int d_v, int causal, int p_mode,
+                        int block_scale, void* stream) {
+    int rc = check_common(q, k, v, out, B, Hq, Hkv, N, d_qk, d_v, causal, 1);
+    if (rc <= 0) return rc;
+    if (p_mode != ZYFA_P_EXACT && p_mode != ZYFA_P_LEAN) return ZYFA_ERR_UNSUPPORTED;
+    if (block_scale != 0 && block_scale != 1) return ZYFA_ERR_UNSUPPORTED;
+    if (!aligned(descale_q, 4) || !aligned(descale_k, 4) || !aligned(descale_v, 4))
+        return ZYFA_ERR_ALIGN;
+    FwdArgs a{out, descale_q, descale_k, descale_v, B, Hq, Hkv, N, p_mode, block_scale,
+              1.0f / sqrtf(static_cast<float>(d_qk))};
+    auto s = static_cast<cudaStream_t>(stream);
+    return d_qk == 128 ? launch<true, 128>(q, k, v, a, s) : launch<true, 192>(q, k, v, a, s);
+}
+
+extern "C" int zyfa_fwd_bf16(const void* q, const void* k, const void* v, void* out, int B,
+                             int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
+                             void* stream) {
+    int rc = check_common(q, k, v, out, B, Hq, Hkv, N, d_qk, d_v, causal, 2);
+    if (rc <= 0) return rc;
+    FwdArgs a{out, nullptr, nullptr, nullptr, B, Hq, Hkv, N, 0, 0,
+              1.0f / sqrtf(static_cast<float>(d_qk))};
+    auto s = static_cast<cudaStream_t>(stream);
+    return d_qk == 128 ? launch<false, 128>(q, k, v, a, s) : launch<false, 192>(q, k, v, a, s);
+}
+
+extern "C" const char* zyfa_status_string(int status) {
+    switch (status) {
+        case ZYFA_OK: return "ok";
+        case ZYFA_ERR_NULL: return "a required pointer is NULL";
+        case ZYFA_ERR_SHAPE: return "invalid shape (sizes, Hq % Hkv, N % 128 or size limits)";
+        case ZYFA_ERR_UNSUPPORTED: return "unsupported configuration (causal, head dims or mode)";
+        case ZYFA_ERR_ALIGN: return "misaligned pointer (tensors need 16 bytes, scales 4)";
+        case ZYFA_ERR_CUDA: return "CUDA launch or driver call failed";
+        case ZYFA_ERR_TIMEOUT: return "a device-side wait ran out of time";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int zyfa_last_device_status(void* stream) {
+    auto s = static_cast<cudaStream_t>(stream);
+    int v = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return ZYFA_ERR_CUDA;
+    if (cudaMemcpyFromSymbolAsync(&v, zyfa::g_device_status, sizeof(int), 0,
+                                  cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return ZYFA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return ZYFA_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbolAsync(zyfa::g_device_status, &zero, sizeof(int), 0,
+                                    cudaMemcpyHostToDevice, s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess)
+            return ZYFA_ERR_CUDA;
+        return ZYFA_ERR_TIMEOUT;
+    }
+    return ZYFA_OK;
+}
+
+extern "C" int zyfa_version(void) { return 100; }

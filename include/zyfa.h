@@ -1,0 +1,104 @@
+/*
+ * zyfa.h -- C ABI of the GB300 (sm_103a) causal attention forward library.
+ *
+ * The operation is the causal FlashAttention forward (prefill) pass of
+ * "ZYFA: Speed and Accuracy of FP8 FlashAttention on AMD CDNA4"
+ * (arXiv 2611.07496):
+ *
+ *     O = softmax(c Q K^T + M) V,   c = 1/sqrt(d_qk),  M the causal mask
+ *                                   (Sec. II-B),
+ *
+ * computed FlashAttention-style over blocks of 128 keys with a running row
+ * maximum in base-2 units and lazy rescaling (Sec. II-B; Sec. IV-A "Lazy
+ * rescaling": tau = 0.125 in FP8, 0.5 in BF16 at d_qk = 128, 8 in BF16 at
+ * d_qk = 192).  In FP8 the inputs are e4m3 codes with one FP32 scale per
+ * tensor (Sec. II-C); each probability is rounded to e4m3 before the PV
+ * product either by Lean P, the code y = 8(x + 6 + 7) - 0.35 rounded to an
+ * integer (Sec. IV-B1, Eq. 2), or by exact P, e4m3(2^(x+6)); each block of 64
+ * keys of a row is scaled by 2^o, o the whole binades between the block
+ * maximum and the row maximum, and the PV product by 2^-o (Sec. IV-B2); the
+ * output divides by the sum of the rounded probabilities (Sec. IV-B3).
+ *
+ * Common conventions
+ *   - Layout: contiguous BSHD.  q [B, N, Hq, d_qk], k [B, N, Hkv, d_qk],
+ *     v [B, N, Hkv, d_v], out [B, N, Hq, d_v].  Query head h reads key/value
+ *     head h / (Hq / Hkv) (grouped-query attention, Table VI).
+ *   - Supported: causal = 1; N a multiple of 128; (d_qk, d_v) = (128, 128)
+ *     or (192, 128); Hq a multiple of Hkv.
+ *   - Ownership: every buffer is device memory owned by the caller.  The
+ *     library allocates no device memory per call, keeps no pointer after
+ *     the call returns and writes nothing but `out`.
+ *   - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and the call returns without synchronising.
+ *   - Errors: a bad argument returns a negative status before anything is
+ *     launched; a failed launch returns ZYFA_ERR_CUDA.  Every wait inside the
+ *     kernel is bounded (about 1.5 s); a wait that runs out ends the kernel
+ *     early and is reported by zyfa_last_device_status().
+ *   - B = 0 or N = 0 is an empty problem: ZYFA_OK, nothing launched, the
+ *     pointers are not inspected.
+ */
+#ifndef ZYFA_H
+#define ZYFA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ZYFA_OK = 0,
+    ZYFA_ERR_NULL = -1,         /* a required pointer is NULL                     */
+    ZYFA_ERR_SHAPE = -2,        /* negative/zero sizes, Hq % Hkv, N % 128, limits */
+    ZYFA_ERR_UNSUPPORTED = -3,  /* causal != 1, head dims, p_mode / block_scale   */
+    ZYFA_ERR_ALIGN = -4,        /* a tensor not 16-byte aligned, a scale not 4    */
+    ZYFA_ERR_CUDA = -5,         /* launch or driver call failed                   */
+    ZYFA_ERR_TIMEOUT = -6       /* a device-side wait ran out (see below)         */
+} zyfa_status;
+
+enum { ZYFA_P_EXACT = 0, ZYFA_P_LEAN = 1 };
+
+/*
+ * FP8 e4m3 causal attention forward.
+ *   q, k, v      e4m3 ("fn" variant) codes, one byte per element, BSHD.
+ *   descale_q/k/v  pointers to one FP32 value each in device memory: the
+ *                scale that maps a code back to its real value; NULL means
+ *                1.0.  They enter the score scale c*dq*dk and the output.
+ *   out          BF16 output, BSHD, d_v = 128 (round to nearest even).
+ *   p_mode       ZYFA_P_LEAN (Eq. 2) or ZYFA_P_EXACT.
+ *   block_scale  1: per-64-key power-of-two scaling (Sec. IV-B2); 0: o = 0.
+ *   stream       cudaStream_t the kernel is launched on.
+ * Returns a zyfa_status.
+ */
+int zyfa_fwd(const void* q, const void* k, const void* v,
+             const float* descale_q, const float* descale_k, const float* descale_v,
+             void* out, int B, int Hq, int Hkv, int N, int d_qk, int d_v,
+             int causal, int p_mode, int block_scale, void* stream);
+
+/*
+ * BF16 causal attention forward (the comparison path of Sec. IV-D): q, k, v
+ * and out are BF16, BSHD.  Probabilities p = 2^(t - m) are computed in FP32,
+ * rounded to BF16 for the PV product, and the row sum adds the unrounded p.
+ * Same conventions and status codes as zyfa_fwd.
+ */
+int zyfa_fwd_bf16(const void* q, const void* k, const void* v, void* out,
+                  int B, int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
+                  void* stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char* zyfa_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reports and clears the device status word of
+ * the current device: ZYFA_ERR_TIMEOUT if any kernel of this library has had
+ * a bounded wait run out since the last call, else ZYFA_OK (or
+ * ZYFA_ERR_CUDA if the synchronisation itself failed).
+ */
+int zyfa_last_device_status(void* stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int zyfa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZYFA_H */

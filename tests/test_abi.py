@@ -1,0 +1,93 @@
+"""The C ABI library builds, loads and exports every symbol include/zyfa.h
+declares; argument errors are reported before anything is launched.  No
+compute call is made here, so these run without a GPU."""
+import os
+import re
+
+import pytest
+
+import fp8_causal_flashattention_gb300 as Z
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    Z.build()
+    return Z.load()
+
+
+def _declared():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(zyfa_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert {"zyfa_fwd", "zyfa_fwd_bf16", "zyfa_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(Z.EXPORTS) <= set(names)
+
+
+def test_status_strings(lib):
+    for s in range(0, -7, -1):
+        assert Z.zyfa_status_string(s) != "unknown status"
+    assert Z.zyfa_status_string(-99) == "unknown status"
+    assert Z.zyfa_version() >= 100
+
+
+FAKE = 1 << 20          # 16-byte aligned, never dereferenced: checks fail first
+
+
+@pytest.mark.parametrize("args,want", [
+    (dict(N=100), Z.ZYFA_ERR_SHAPE),               # N % 128
+    (dict(Hq=3, Hkv=2), Z.ZYFA_ERR_SHAPE),         # Hq % Hkv
+    (dict(B=-1), Z.ZYFA_ERR_SHAPE),
+    (dict(Hq=0), Z.ZYFA_ERR_SHAPE),
+    (dict(causal=0), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(d_qk=64), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(d_v=192), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(p_mode=2), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(block_scale=3), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(q=0), Z.ZYFA_ERR_NULL),
+    (dict(out=0), Z.ZYFA_ERR_NULL),
+    (dict(k=FAKE + 8), Z.ZYFA_ERR_ALIGN),
+    (dict(dq=FAKE + 2), Z.ZYFA_ERR_ALIGN),
+    (dict(N=1 << 30, Hq=1 << 11, Hkv=1), Z.ZYFA_ERR_SHAPE),   # byte stride >= 2^40
+])
+def test_fp8_argument_errors(lib, args, want):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, dq=None, dk=None, dv=None, out=FAKE, B=1, Hq=2, Hkv=1,
+             N=256, d_qk=128, d_v=128, causal=1, p_mode=1, block_scale=1)
+    a.update(args)
+    rc = lib.zyfa_fwd(a["q"], a["k"], a["v"], a["dq"], a["dk"], a["dv"], a["out"], a["B"],
+                      a["Hq"], a["Hkv"], a["N"], a["d_qk"], a["d_v"], a["causal"],
+                      a["p_mode"], a["block_scale"], None)
+    assert rc == want
+
+
+@pytest.mark.parametrize("args,want", [
+    (dict(N=64), Z.ZYFA_ERR_SHAPE),
+    (dict(causal=2), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(v=0), Z.ZYFA_ERR_NULL),
+    (dict(out=FAKE + 4), Z.ZYFA_ERR_ALIGN),
+])
+def test_bf16_argument_errors(lib, args, want):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, B=2, Hq=4, Hkv=4, N=512, d_qk=192, d_v=128,
+             causal=1)
+    a.update(args)
+    rc = lib.zyfa_fwd_bf16(a["q"], a["k"], a["v"], a["out"], a["B"], a["Hq"], a["Hkv"],
+                           a["N"], a["d_qk"], a["d_v"], a["causal"], None)
+    assert rc == want
+
+
+@pytest.mark.parametrize("B,N", [(0, 256), (2, 0)])
+def test_empty_problem_is_ok_without_launch(lib, B, N):
+    assert lib.zyfa_fwd(None, None, None, None, None, None, None, B, 4, 4, N, 128, 128,
+                        1, 1, 1, None) == Z.ZYFA_OK
+    assert lib.zyfa_fwd_bf16(None, None, None, None, B, 4, 4, N, 128, 128, 1, None) == Z.ZYFA_OK
