@@ -1,0 +1,363 @@
+"""Benchmark of the causal FP8 attention forward on one GB300 (per GPU rank).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload d128] [--mode lean]
+
+One step = one causal attention forward over the whole workload (the
+configuration the metric is quoted on: B=1, Hq=Hkv=32, N=32768,
+d_qk=d_v=128, FP8 e4m3 with Lean P and per-64-key block scaling), inputs
+resident in HBM.  Prints one JSON line (rank 0).  Throughput is the causal
+FLOP count F = 2 B Hq N^2 (d_qk + d_v) / 2 ("ZYFA", Eq. 1) over the mean
+device time of one launch, timed with CUDA events on the launching stream.
+
+--impl reference times the CPU oracle (the tests' reference implementation)
+on the host cores, on bounded samples of query rows of the same workload.
+Multi-GPU runs are replicas: every rank runs the whole workload on its own
+GPU (no collective on the data path); value = all ranks' FLOPs / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic as S  # noqa: E402
+
+METRIC = "FP8 causal prefill attn TFLOPS (N=32K, d=128 and MLA 192/128), % of FP8 peak"
+UNIT = "TFLOP/s"
+FP8_OVER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor ratio (4.5 / 2.25 PF)
+KERNEL_SOURCES = ["fp8_causal_flashattention_gb300/csrc/fwd.cuh",
+                  "fp8_causal_flashattention_gb300/csrc/ptx.cuh",
+                  "fp8_causal_flashattention_gb300/csrc/zyfa_api.cu"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def row_flops(wl: S.Workload, rows) -> float:
+    i = np.asarray(rows) % wl.N
+    return float(np.sum(2.0 * (i + 1) * (wl.d_qk + wl.d_v)))
+
+
+# --------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# --------------------------------------------------------------------------
+def oracle_sample(wl: S.Workload, inp: S.Inputs, mode: str, target_s: float, seed: int):
+    """Times the oracle on a random sample of rows sized for ~target_s."""
+    import oracle
+    from tests import parity as P
+    p = P.oracle_params(wl, inp, mode)
+    q, k, v = P.qkv_for(inp, mode)
+    rng = np.random.default_rng(seed)
+    total = wl.B * wl.Hq * wl.N
+    nthreads = oracle.default_threads()
+    probe = rng.choice(total, 256, replace=False)
+    t0 = time.perf_counter()
+    oracle.fwd(p, q, k, v, probe, nthreads)
+    rate = row_flops(wl, probe) / max(time.perf_counter() - t0, 1e-6)
+    n = int(np.clip(target_s * rate / (row_flops(wl, probe) / 256), 64, total))
+    rows = rng.choice(total, n, replace=False)
+    t0 = time.perf_counter()
+    oracle.fwd(p, q, k, v, rows, nthreads)
+    dt = time.perf_counter() - t0
+    return row_flops(wl, rows) / dt / 1e12, {"rows": int(n), "seconds": dt, "threads": nthreads}
+
+
+def run_reference(args, wl: S.Workload):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    inp = S.make_inputs(wl)
+    vals = []
+    info = None
+    step_s = 0.25 if args.steps > 50 else 1.5
+    for i in range(args.warmup + args.steps):
+        v, info = oracle_sample(wl, inp, args.mode, step_s, seed=100 + i)
+        if i >= args.warmup:
+            vals.append(v)
+    value = float(np.mean(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic",
+        "config": config_dict(wl, args),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": info["threads"], "kind": "oracle",
+                         "sample": f"each step: {info['rows']} random query rows of the workload "
+                                   f"(~{step_s}s of CPU work), TFLOP/s = sum 2(i+1)(d_qk+d_v) / time"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# GPU
+# --------------------------------------------------------------------------
+def config_dict(wl: S.Workload, args) -> dict:
+    return {"workload": f"{wl.name}: B={wl.B} Hq={wl.Hq} Hkv={wl.Hkv} N={wl.N} d_qk={wl.d_qk} "
+                        f"d_v={wl.d_v} causal, FP8 e4m3 {args.mode}",
+            "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "N": wl.N, "d_qk": wl.d_qk, "d_v": wl.d_v,
+            "mode": args.mode, "inputs": "N(0,1) -> per-tensor e4m3 (descale amax/448)",
+            "l2": "inputs larger than L2 (no flush)"}
+
+
+class ClockSampler:
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus = bus_id
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.strip()]
+        if self.bus:
+            mine = [r for r in rows if len(r) > 1 and r[1].lower().endswith(self.bus.lower())]
+            rows = mine or rows
+        if rows and len({r[0] for r in rows}) > 1:
+            first = rows[0][0]
+            rows = [r for r in rows if r[0] == first]
+        num = lambda x: x.replace(".", "", 1).isdigit()  # noqa: E731
+        sm = [float(r[2]) for r in rows if len(r) > 2 and num(r[2])]
+        mx = [float(r[3]) for r in rows if len(r) > 3 and num(r[3])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in rows for j in range(4)
+                          if len(r) > 6 + j and r[6 + j].strip() == "Active"})
+        pw = [float(r[4]) for r in rows if len(r) > 4 and num(r[4])]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(sm), "power_w_max": max(pw) if pw else None}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def stored_traffic(name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(name)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def time_launches(fn, steps, warmup, stream):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_ours(args, wl: S.Workload):
+    import torch
+    import fp8_causal_flashattention_gb300 as Z
+    from tests import parity as P
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    Z.load()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    inp = S.make_inputs(wl)
+    (q, k, v), ds = P.to_device(inp)
+    out = torch.empty((wl.B, wl.N, wl.Hq, wl.d_v), dtype=torch.bfloat16, device=dev)
+    p_mode = Z.ZYFA_P_LEAN if args.mode.startswith("lean") else Z.ZYFA_P_EXACT
+    bs = 0 if args.mode.endswith("nobs") else 1
+
+    def step():
+        rc = Z.zyfa_fwd(q, k, v, ds[0], ds[1], ds[2], out, wl.B, wl.Hq, wl.Hkv, wl.N, wl.d_qk,
+                        wl.d_v, 1, p_mode, bs, stream)
+        if rc != Z.ZYFA_OK:
+            raise Z.ZyfaError(rc, "zyfa_fwd")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    props = torch.cuda.get_device_properties(local)
+    bus = None
+    if hasattr(props, "pci_bus_id"):
+        bus = "%02X:%02X.0" % (props.pci_bus_id, getattr(props, "pci_device_id", 0))
+    clk = ClockSampler(bus)
+    clk.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    status = Z.zyfa_last_device_status()
+    if status != Z.ZYFA_OK:
+        raise RuntimeError(f"device status {status}")
+    flops = wl.causal_flops
+    value = flops * ws / (ms * 1e-3) / 1e12
+
+    # parity spot check of the timed output (sampled rows against the oracle)
+    rows = S.sample_rows(wl, per_head=16)
+    parity = P.errors(P.gather_rows(out, wl, rows), inp, args.mode, rows, extra=False)
+
+    # end to end through the C ABI: pinned host inputs -> device, kernel,
+    # output -> pinned host, every step
+    hq, hk, hv = (torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+                  for a in (inp.q8, inp.k8, inp.v8))
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 30))
+    e2e_ms = time_launches(e2e_step, e2e_steps, 2, stream)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = hout.numel() * hout.element_size()
+
+    peaks, peak_src = measured_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    achieved = flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+        "config": config_dict(wl, args),
+        "pct_of_fp8_peak": 100.0 * achieved / fp8_peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": fp8_peak,
+                     "unit": "TFLOP/s", "frac": achieved / fp8_peak,
+                     "traffic": stored_traffic(f"{wl.name}_{args.mode}"),
+                     "peak_source": f"{peak_src}: MEASURED_PEAKS bf16_tflops (burst) x "
+                                    f"{FP8_OVER_BF16} nominal FP8/BF16 ratio",
+                     "algorithmic": "F = B*Hq*N^2*(d_qk+d_v) causal FLOPs per launch"},
+        "e2e": {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "parity": {"rows": parity["rows"], "rel_l2": parity["rel_l2"],
+                   "max_abs_frac": parity["max_abs_frac"]},
+        "kernel_hash": kernel_hash(),
+    }
+    del hq, hk, hv, hout
+    if not args.no_extras:
+        line["also"] = extras(args, P, fp8_peak, peaks["bf16_tflops"])
+    if rank == 0 and not args.no_cpu_baseline:
+        v_cpu, info = oracle_sample(wl, inp, args.mode, args.cpu_seconds, seed=7)
+        line["cpu_baseline"] = {
+            "value": v_cpu, "unit": UNIT, "cores": info["threads"], "kind": "oracle",
+            "sample": f"{info['rows']} random query rows of the workload, "
+                      f"{info['seconds']:.1f} s; TFLOP/s = sum 2(i+1)(d_qk+d_v) / time"}
+    if ws > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def extras(args, P, fp8_peak, bf16_peak):
+    """The other measured points: BF16 and exact P at d=128, and the MLA shape
+    (exact P, the paper's default there, and Lean P), device-timed alike."""
+    import torch
+    res = {}
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps // 4, 50))
+    for name, mode in (("d128", "bf16"), ("d128", "exact"), ("mla", "exact"), ("mla", "lean")):
+        wl = S.WORKLOADS[name]
+        inp = S.make_inputs(wl, fp8=mode != "bf16", bf16=mode == "bf16")
+        dev = P.to_device(inp, mode != "bf16")
+        ms = time_launches(lambda: P.gpu_run(inp, mode, dev), steps, 3, stream)
+        tf = wl.causal_flops / (ms * 1e-3) / 1e12
+        peak = bf16_peak if mode == "bf16" else fp8_peak
+        res[f"{name}_{mode}"] = {"tflops": tf, "ms": ms, "frac_of_peak": tf / peak}
+        del dev, inp
+        torch.cuda.empty_cache()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="d128", choices=sorted(S.WORKLOADS))
+    ap.add_argument("--mode", default="lean", choices=["lean", "exact", "lean_nobs", "exact_nobs"])
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    wl = S.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

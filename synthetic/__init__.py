@@ -110,7 +110,7 @@ class Workload:
     N: int
     d_qk: int
     d_v: int
-    kind: str = "gaussian"          # "gaussian" or "activation"
+    kind: str = "gaussian"          # "gaussian", "activation" or "sink"
     note: str = ""
 
     @property
@@ -167,6 +167,8 @@ def fp32_qkv(wl: Workload, seed: int = SEED):
     meta = {}
     if wl.kind == "activation":
         q, k, meta = _activation_like(wl, q, k, seed)
+    elif wl.kind == "sink":
+        q, k, meta = _sink(wl, q, k)
     return q, k, v, meta
 
 
@@ -257,3 +259,22 @@ def _activation_like(wl: Workload, q, k, seed: int):
         "far16_share": _far_share(q, k, wl, 1.0, rows, 16.0),
     }
     return q, k, meta
+
+
+# --------------------------------------------------------------------------
+# sink inputs
+# --------------------------------------------------------------------------
+SINK_GAP = 14.0              # base-2 score of the sink key above the Gaussian part
+
+
+def _sink(wl: Workload, q, k, gap: float = SINK_GAP):
+    """Key 0 of every (batch, KV head) is a sink: channel 0 of every query is
+    4 and channel 0 of key 0 is set so that the sink's base-2 score sits about
+    ``gap`` above the rest; channel 0 of the other keys is 0.  Every later
+    64-key block then lies roughly gap - 2 ... gap binades below the row
+    maximum, with a per-row spread."""
+    c = np.log2(np.e) / np.sqrt(wl.d_qk)
+    q[..., 0] = 4.0
+    k[:, :, :, 0] = 0.0
+    k[:, 0, :, 0] = np.float32(gap / (c * 4.0))
+    return q, k, {"sink_gap": gap}
