@@ -16,13 +16,18 @@
 //   - row sum of the rounded probabilities by one extra MMA against ones:
 //     Sec. IV-B3.
 //
-// GB300 mapping (one CTA per 128-row query tile, 192 threads):
-//   warps 0-3  softmax: thread r owns query row r (TMEM lane r);
-//   warp 4     TMA producer: Q tile once, then a ring of K/V stages;
-//   warp 5     TMEM allocator and MMA issuer (one elected thread).
-// TMEM (512 columns): S0 [0,128), S1 [128,256) double-buffered scores (P is
-// written over the first 32 / 64 columns of its S buffer), O [256,384),
-// L [384,400) row sums, SFA [400,404)/[404,408) A scale factors, SFB [408,412).
+// GB300 mapping (one CTA per 128-row query tile, 320 threads):
+//   warps 0-7  softmax, two warpgroups: warpgroup w takes the key blocks
+//              i = w (mod 2) and its thread r owns query row r (TMEM lane r);
+//              the running maximum after each block is handed to the other
+//              warpgroup through shared memory and an mbarrier, so the two
+//              work on consecutive blocks at the same time;
+//   warp 8     TMA producer: Q tile once, then a ring of K/V stages;
+//   warp 9     TMEM allocator and MMA issuer (one elected thread).
+// TMEM (512 columns): S0 [0,128), S1 [128,256) double-buffered scores,
+// O [256,384), P0/P1 double-buffered probabilities (FP8: [384,416)/[416,448),
+// BF16: [384,448)/[448,512)); FP8 also L [448,464) row sums, SFA
+// [464,468)/[468,472) A scale factors and SFB [472,476).
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -51,6 +56,11 @@ struct FwdArgs {
 
 template <bool FP8, int DQK>
 struct FwdCfg {
+    // two softmax warpgroups; warpgroup w takes the key blocks i = w (mod 2)
+    static constexpr int NWG = 2;
+    static constexpr int NSM = 128 * NWG;     // softmax threads
+    static constexpr int WARP_TMA = 4 * NWG;  // producer warp
+    static constexpr int WARP_MMA = 4 * NWG + 1;   // TMEM owner and MMA issuer
     static constexpr int BM = 128;            // query rows per tile
     static constexpr int BN = 128;            // keys per block
     static constexpr int DV = 128;
@@ -70,17 +80,24 @@ struct FwdCfg {
     static constexpr int OFF_K = OFF_Q + Q_BYTES;
     static constexpr int OFF_V = OFF_K + NST * K_BYTES;
     static constexpr int OFF_ONES = OFF_V + NST * V_BYTES;
-    static constexpr int OFF_BAR = OFF_ONES + ONES_BYTES;
+    static constexpr int OFF_XCH = OFF_ONES + ONES_BYTES;       // running max [2][128]
+    static constexpr int XCH_BYTES = 2 * 128 * 4;
+    static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
     // barriers: q_full, k_full[NST], v_full[NST], kv_empty[NST], s_full[2],
-    // p_full[2], o_done, mma_done; then the TMEM slot and the abort flag
-    static constexpr int NBAR = 1 + 3 * NST + 2 + 2 + 1 + 1;
+    // p_full[2], o_done[2] (PV of even / odd blocks), mma_done, m_ready[2]
+    // (running max of even / odd blocks published), fin (last PV seen),
+    // s_free[2] (S of even / odd blocks loaded); then the TMEM slot and the
+    // abort flag
+    static constexpr int NBAR = 1 + 3 * NST + 2 + 2 + 2 + 1 + 2 + 1 + 2;
     static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16;
-    static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;        // alignment slack
+    static constexpr int SMEM_ALLOC = SMEM_BYTES;   // base is 1024-aligned (checked)
     static constexpr float TAU = FP8 ? kTauFp8 : (DQK == 192 ? 8.0f : 0.5f);
-    static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_L = 384;
-    static constexpr uint32_t COL_SFA0 = 400, COL_SFA1 = 404, COL_SFB = 408;
+    // P has its own double buffer, so S_i is free once it has been loaded
+    static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
+    static constexpr uint32_t COL_P0 = 384, COL_P1 = FP8 ? 416 : 448;
+    static constexpr uint32_t COL_L = 448, COL_SFA0 = 464, COL_SFA1 = 468, COL_SFB = 472;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr int THREADS = 192;
+    static constexpr int THREADS = NSM + 64;
 };
 
 __device__ __forceinline__ float fma_sat(float a, float b, float c) {
@@ -120,20 +137,34 @@ __device__ __forceinline__ uint32_t lean_word(float s, float a, float b) {
     return __float_as_uint(fmaf(z, 256.0f, 12582912.0f));
 }
 
+// Named barrier over the softmax warps that also ANDs a predicate across
+// them, so that every thread takes the same branch afterwards.
+__device__ __forceinline__ bool bar_and(int id, int nthreads, bool pred) {
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "bar.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r) : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+                 : "memory");
+    return r != 0;
+}
+
 template <bool FP8, int DQK>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(FwdCfg<FP8, DQK>::THREADS, 1)
 zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
     using C = FwdCfg<FP8, DQK>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
+    if (sbase & 1023u) {   // swizzled TMA / MMA operands need 1 KB alignment
+        if (threadIdx.x == 0) atomicCAS(&g_device_status, 0, (9 << 8) | 2);
+        return;
+    }
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     const uint32_t bar0 = smem_u32(bars);
     auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
     const int B_QF = 0, B_KF = 1, B_VF = 1 + C::NST, B_KE = 1 + 2 * C::NST;
-    const int B_SF = 1 + 3 * C::NST, B_PF = B_SF + 2, B_OD = B_PF + 2, B_MD = B_OD + 1;
+    const int B_SF = 1 + 3 * C::NST, B_PF = B_SF + 2, B_OD = B_PF + 2, B_MD = B_OD + 2;
+    const int B_MR = B_MD + 1, B_FIN = B_MR + 2, B_SX = B_FIN + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -160,18 +191,22 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int s = 0; s < 2; ++s) {
             mbar_init(BAR(B_SF + s), 1);
             mbar_init(BAR(B_PF + s), 128);
+            mbar_init(BAR(B_MR + s), 128);
+            mbar_init(BAR(B_SX + s), 128);
         }
         mbar_init(BAR(B_OD), 1);
+        mbar_init(BAR(B_OD + 1), 1);
         mbar_init(BAR(B_MD), 1);
+        mbar_init(BAR(B_FIN), 128);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == C::WARP_MMA) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
     }
     if constexpr (FP8) {
-        if (warp == 4) {   // B operand of the row-sum MMA: e4m3 ones (0x38)
+        if (warp == C::WARP_TMA) {   // B operand of the row-sum MMA: e4m3 ones (0x38)
             uint32_t* ones = reinterpret_cast<uint32_t*>(smem + C::OFF_ONES);
             for (int i = lane; i < C::ONES_BYTES / 4; i += 32) ones[i] = 0x38383838u;
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -182,230 +217,318 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
+    // Producer and MMA warps run their loops warp-uniformly (every lane
+    // computes the same coordinates and descriptors); elect.sync picks the
+    // lane that issues each TMA copy, MMA and commit.
+    auto wait_warp = [&](int bar, uint32_t parity, int site) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(BAR(bar), parity, abort_flag, site));
+    };
+    if (warp == C::WARP_TMA) {
         // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            mbar_expect_tx(BAR(B_QF), C::Q_BYTES);
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        mbar_expect_tx_elect(BAR(B_QF), C::Q_BYTES);
+        #pragma unroll
+        for (int c = 0; c < C::NCH; ++c)
+            tma_load_4d_elect(sbase + C::OFF_Q + c * (C::BM * C::CB), &tm_q, BAR(B_QF),
+                              c * C::CB / C::ESZ, h, qt * C::BM, b);
+        int issued = 0;
+        for (int i = 0; i < nblk; ++i) {
+            const int st = i % C::NST;
+            if (i >= C::NST && !wait_warp(B_KE + st, ((i / C::NST) - 1) & 1, 1)) break;
+            mbar_expect_tx_elect(BAR(B_KF + st), C::K_BYTES);
+            #pragma unroll
             for (int c = 0; c < C::NCH; ++c)
-                tma_load_4d(sbase + C::OFF_Q + c * (C::BM * C::CB), &tm_q, BAR(B_QF),
-                            c * C::CB / C::ESZ, h, qt * C::BM, b);
-            int issued = 0;
-            for (int i = 0; i < nblk; ++i) {
+                tma_load_4d_elect(sbase + C::OFF_K + st * C::K_BYTES + c * (C::BN * C::CB), &tm_k,
+                                  BAR(B_KF + st), c * C::CB / C::ESZ, g, i * C::BN, b);
+            mbar_expect_tx_elect(BAR(B_VF + st), C::V_BYTES);
+            #pragma unroll
+            for (int c = 0; c < C::VCH; ++c)
+                tma_load_4d_elect(sbase + C::OFF_V + st * C::V_BYTES + c * (C::BN * 128), &tm_v,
+                                  BAR(B_VF + st), c * 128 / C::ESZ, g, i * C::BN, b);
+            ++issued;
+        }
+        if (*abort_flag) {
+            // let the loads still in flight land before the CTA exits
+            for (int i = issued - C::NST < 0 ? 0 : issued - C::NST; i < issued; ++i) {
                 const int st = i % C::NST;
-                if (i >= C::NST &&
-                    !mbar_wait(BAR(B_KE + st), ((i / C::NST) - 1) & 1, abort_flag, 1))
-                    break;
-                mbar_expect_tx(BAR(B_KF + st), C::K_BYTES);
-                for (int c = 0; c < C::NCH; ++c)
-                    tma_load_4d(sbase + C::OFF_K + st * C::K_BYTES + c * (C::BN * C::CB), &tm_k,
-                                BAR(B_KF + st), c * C::CB / C::ESZ, g, i * C::BN, b);
-                mbar_expect_tx(BAR(B_VF + st), C::V_BYTES);
-                for (int c = 0; c < C::VCH; ++c)
-                    tma_load_4d(sbase + C::OFF_V + st * C::V_BYTES + c * (C::BN * 128), &tm_v,
-                                BAR(B_VF + st), c * 128 / C::ESZ, g, i * C::BN, b);
-                ++issued;
-            }
-            if (*abort_flag) {
-                // let the loads still in flight land before the CTA exits
-                for (int i = issued - C::NST < 0 ? 0 : issued - C::NST; i < issued; ++i) {
-                    const int st = i % C::NST;
-                    const uint32_t ph = (i / C::NST) & 1;
-                    unsigned long long t0 = globaltimer();
-                    while (!mbar_try(BAR(B_KF + st), ph) && globaltimer() - t0 < kWaitBudgetNs) {}
-                    while (!mbar_try(BAR(B_VF + st), ph) && globaltimer() - t0 < kWaitBudgetNs) {}
-                }
+                const uint32_t ph = (i / C::NST) & 1;
+                unsigned long long t0 = globaltimer();
+                while (!mbar_try(BAR(B_KF + st), ph) && globaltimer() - t0 < kWaitBudgetNs) {}
+                while (!mbar_try(BAR(B_VF + st), ph) && globaltimer() - t0 < kWaitBudgetNs) {}
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == C::WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t kQK = idesc_dense(FP8 ? kFmtE4M3 : kFmtBF16,
-                                                 FP8 ? kFmtE4M3 : kFmtBF16, 0, 0, 128, 128);
-            constexpr uint32_t kPV16 = idesc_dense(kFmtBF16, kFmtBF16, 0, 1, 128, 128);
-            bool ok = mbar_wait(BAR(B_QF), 0, abort_flag, 2);
-            auto issue_qk = [&](int i) -> bool {
-                const int st = i % C::NST;
-                if (!mbar_wait(BAR(B_KF + st), (i / C::NST) & 1, abort_flag, 3)) return false;
-                tc_fence_after();
-                const uint32_t d = tmem + ((i & 1) ? C::COL_S1 : C::COL_S0);
-                #pragma unroll
-                for (int kk = 0; kk < C::QK_STEPS; ++kk) {
-                    const int off = kk * 32;
-                    const int ch = off / C::CB, in = off % C::CB;
-                    const uint64_t a = smem_desc(sbase + C::OFF_Q + ch * (C::BM * C::CB) + in,
-                                                 16, 8 * C::CB, C::SWZ);
-                    const uint64_t bk = smem_desc(
-                        sbase + C::OFF_K + st * C::K_BYTES + ch * (C::BN * C::CB) + in,
-                        16, 8 * C::CB, C::SWZ);
-                    mma_ss<FP8 ? 1 : 0>(d, a, bk, kQK, kk > 0 ? 1u : 0u);
-                }
-                tc_commit(BAR(B_SF + (i & 1)));
-                return true;
-            };
-            auto issue_pv = [&](int i) -> bool {
-                const int st = i % C::NST;
-                if (!mbar_wait(BAR(B_PF + (i & 1)), (i >> 1) & 1, abort_flag, 4)) return false;
-                if (!mbar_wait(BAR(B_VF + st), (i / C::NST) & 1, abort_flag, 5)) return false;
-                tc_fence_after();
-                const uint32_t p_col = tmem + ((i & 1) ? C::COL_S1 : C::COL_S0);
-                const uint32_t vbase = sbase + C::OFF_V + st * C::V_BYTES;
-                #pragma unroll
-                for (int kk = 0; kk < C::PV_STEPS; ++kk) {
-                    const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                    if constexpr (FP8) {
-                        // 32 keys per MMA: V rows of 128 bytes, 8-row groups 1 KB apart
-                        const uint64_t bv = smem_desc(vbase + kk * 32 * 128, 1024, 1024,
-                                                      kSwizzle128B);
-                        const uint64_t b1 = smem_desc(sbase + C::OFF_ONES + kk * 32, 16, 1024,
-                                                      kSwizzle128B);
-                        const uint32_t sfa = tmem + ((i & 1) ? C::COL_SFA1 : C::COL_SFA0);
-                        const uint32_t sfb = tmem + C::COL_SFB;
-                        mma_ts_mx8(tmem + C::COL_O, p_col + kk * 8, bv,
-                                   idesc_mx(kFmtE4M3, kFmtE4M3, 0, 1, 128, 128, kk, kk), sfa, sfb,
-                                   acc);
-                        mma_ts_mx8(tmem + C::COL_L, p_col + kk * 8, b1,
-                                   idesc_mx(kFmtE4M3, kFmtE4M3, 0, 0, 128, 16, kk, kk), sfa, sfb,
-                                   acc);
-                    } else {
-                        // 16 keys per MMA; the two 64-column halves of V are 16 KB apart
-                        const uint64_t bv = smem_desc(vbase + kk * 16 * 128, C::BN * 128, 1024,
-                                                      kSwizzle128B);
-                        mma_ts_f16(tmem + C::COL_O, p_col + kk * 8, bv, kPV16, acc);
-                    }
-                }
-                tc_commit(BAR(B_OD));
-                tc_commit(BAR(B_KE + st));
-                return true;
-            };
-            if (ok) ok = issue_qk(0);
-            for (int i = 0; ok && i < nblk; ++i) {
-                if (i + 1 < nblk) ok = issue_qk(i + 1);
-                if (ok) ok = issue_pv(i);
+        constexpr uint32_t kQK = idesc_dense(FP8 ? kFmtE4M3 : kFmtBF16,
+                                             FP8 ? kFmtE4M3 : kFmtBF16, 0, 0, 128, 128);
+        constexpr uint32_t kPV16 = idesc_dense(kFmtBF16, kFmtBF16, 0, 1, 128, 128);
+        // descriptors of the operand bases; a K step or stage only adds its
+        // byte offset / 16 to the start-address field
+        const uint64_t dq0 = smem_desc(sbase + C::OFF_Q, 16, 8 * C::CB, C::SWZ);
+        const uint64_t dk0 = smem_desc(sbase + C::OFF_K, 16, 8 * C::CB, C::SWZ);
+        // V: rows of 128 bytes (8-row groups 1 KB apart); BF16 V has two
+        // 64-column halves 16 KB apart
+        const uint64_t dv0 = smem_desc(sbase + C::OFF_V, FP8 ? 1024 : C::BN * 128, 1024,
+                                       kSwizzle128B);
+        const uint64_t d10 = smem_desc(sbase + C::OFF_ONES, 16, 1024, kSwizzle128B);
+        bool ok = wait_warp(B_QF, 0, 2);
+        auto issue_qk = [&](int i) {
+            const int st = i % C::NST;
+            const uint32_t d = tmem + ((i & 1) ? C::COL_S1 : C::COL_S0);
+            const uint64_t dk = dk0 + static_cast<uint64_t>((st * C::K_BYTES) >> 4);
+            #pragma unroll
+            for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+                const int off = kk * 32;
+                const int ch = off / C::CB, in = off % C::CB;
+                mma_ss_elect<FP8 ? 1 : 0>(
+                    d, dq0 + static_cast<uint64_t>((ch * (C::BM * C::CB) + in) >> 4),
+                    dk + static_cast<uint64_t>((ch * (C::BN * C::CB) + in) >> 4), kQK,
+                    kk > 0 ? 1u : 0u);
             }
-            // every MMA issued must complete before TMEM is released
-            tc_commit(BAR(B_MD));
-            unsigned long long t0 = globaltimer();
-            while (!mbar_try(BAR(B_MD), 0) && globaltimer() - t0 < kWaitBudgetNs) {}
+            tc_commit_elect(BAR(B_SF + (i & 1)));
+        };
+        auto issue_pv = [&](int i) {
+            const int st = i % C::NST;
+            const uint32_t p_col = tmem + ((i & 1) ? C::COL_P1 : C::COL_P0);
+            const uint64_t dv = dv0 + static_cast<uint64_t>((st * C::V_BYTES) >> 4);
+            #pragma unroll
+            for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+                const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                if constexpr (FP8) {
+                    // 32 keys per MMA
+                    const uint32_t sfa = tmem + ((i & 1) ? C::COL_SFA1 : C::COL_SFA0);
+                    const uint32_t sfb = tmem + C::COL_SFB;
+                    mma_ts_mx8_elect(tmem + C::COL_O, p_col + kk * 8, dv + ((kk * 32 * 128) >> 4),
+                                     idesc_mx(kFmtE4M3, kFmtE4M3, 0, 1, 128, 128, kk, kk), sfa,
+                                     sfb, acc);
+                    mma_ts_mx8_elect(tmem + C::COL_L, p_col + kk * 8, d10 + ((kk * 32) >> 4),
+                                     idesc_mx(kFmtE4M3, kFmtE4M3, 0, 0, 128, 16, kk, kk), sfa,
+                                     sfb, acc);
+                } else {
+                    // 16 keys per MMA
+                    mma_ts_f16_elect(tmem + C::COL_O, p_col + kk * 8,
+                                     dv + ((kk * 16 * 128) >> 4), kPV16, acc);
+                }
+            }
+            tc_commit_elect(BAR(B_OD + (i & 1)));
+            tc_commit_elect(BAR(B_KE + st));
+        };
+        // Issue whichever is ready first: QK_q (K_q loaded and, for q >= 2,
+        // S_{q-2} loaded by its warpgroup) or PV_p (P_p written, V_p loaded).
+        // Every tested phase is the next one of its barrier: K stage q can
+        // not be reloaded before PV_q, s_free of block q can not arrive
+        // before QK_q, and P_{p+2} is written only after PV_p completes.
+        int qn = 0, pn = 0;
+        unsigned long long t_prog = globaltimer();
+        while (ok && pn < nblk) {
+            bool did = false;
+            if (qn < nblk && qn < pn + 2 + 1) {
+                const int st = qn % C::NST;
+                bool rdy = mbar_test(BAR(B_KF + st), (qn / C::NST) & 1) &&
+                           (qn < 2 || mbar_test(BAR(B_SX + (qn & 1)), ((qn - 2) >> 1) & 1));
+                if (__all_sync(0xffffffffu, rdy)) {
+                    tc_fence_after();
+                    issue_qk(qn);
+                    ++qn;
+                    did = true;
+                }
+            }
+            if (pn < qn) {
+                const int st = pn % C::NST;
+                bool rdy = mbar_test(BAR(B_PF + (pn & 1)), (pn >> 1) & 1) &&
+                           mbar_test(BAR(B_VF + st), (pn / C::NST) & 1);
+                if (__all_sync(0xffffffffu, rdy)) {
+                    tc_fence_after();
+                    issue_pv(pn);
+                    ++pn;
+                    did = true;
+                }
+            }
+            if (did) {
+                t_prog = globaltimer();
+            } else if (*abort_flag) {
+                ok = false;
+            } else if (globaltimer() - t_prog > kWaitBudgetNs) {
+                *abort_flag = 1;
+                atomicCAS(&g_device_status, 0, (3 << 8) | 1);
+                ok = false;
+            }
         }
+        // every MMA issued must complete before TMEM is released
+        tc_commit_elect(BAR(B_MD));
+        unsigned long long t0 = globaltimer();
+        while (!mbar_try(BAR(B_MD), 0) && globaltimer() - t0 < kWaitBudgetNs) {}
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
-        const int row = threadIdx.x;                        // 0..127 = TMEM lane
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const int wg = warp >> 2;                           // takes blocks i = wg (mod 2)
+        const int row = threadIdx.x & 127;                  // query row = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t t_row = tmem + lane_off;
+        float* mx = reinterpret_cast<float*>(smem + C::OFF_XCH);   // [2][128]
         const float dq = args.descale_q ? *args.descale_q : 1.0f;
         const float dk = args.descale_k ? *args.descale_k : 1.0f;
         const float dv = args.descale_v ? *args.descale_v : 1.0f;
         const float A1 = FP8 ? args.softmax_scale * dq * dk * kLog2e : args.softmax_scale * kLog2e;
         const float a_lean = A1 * (8.0f / 256.0f);
-        if constexpr (FP8) tmem_st4(t_row + C::COL_SFB, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu,
-                                    0x7F7F7F7Fu);
-        float m_run = -INFINITY;
-        float l_run = 0.0f;                                  // BF16 only
+        if constexpr (FP8) {
+            if (wg == 0) tmem_st4(t_row + C::COL_SFB, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu,
+                                  0x7F7F7F7Fu);
+        }
+        float m_own = -INFINITY;                             // max at this warpgroup's last block
+        float l_own = 0.0f;                                  // BF16: row sum of its blocks
         bool ok = true;
-        for (int i = 0; i < nblk; ++i) {
-            ok = mbar_wait(BAR(B_SF + (i & 1)), (i >> 1) & 1, abort_flag, 6);
-            ok = __all_sync(0xffffffffu, ok);
+        for (int i = wg; i < nblk; i += 2) {
+            // S_i: QK_i arrives on s_full[wg]; this warpgroup is its only waiter
+            ok = __all_sync(0xffffffffu, mbar_wait(BAR(B_SF + wg), (i >> 1) & 1, abort_flag, 6));
             if (!ok) break;
             tc_fence_after();
-            const uint32_t t_s = t_row + ((i & 1) ? C::COL_S1 : C::COL_S0);
+            const uint32_t t_s = t_row + (wg ? C::COL_S1 : C::COL_S0);
             float s[128];
-            #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld32(t_s + c * 32, r);
+            {
+                uint32_t r[128];
+                #pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&r[c * 32]));
                 tmem_wait_ld();
                 #pragma unroll
-                for (int j = 0; j < 32; ++j) s[c * 32 + j] = __uint_as_float(r[j]);
+                for (int j = 0; j < 128; ++j) s[j] = __uint_as_float(r[j]);
             }
+            // S_i is in registers: QK_{i+2} may overwrite the buffer
+            tc_fence_before();
+            mbar_arrive(BAR(B_SX + wg));
             if (i == nblk - 1) {                             // diagonal block: key > query
                 #pragma unroll
                 for (int j = 0; j < 128; ++j)
                     if (j > row) s[j] = -INFINITY;
             }
-            float h0 = s[0], h1 = s[64];
+            float hs[2];                                     // raw maxima of the 64-key blocks
             #pragma unroll
-            for (int j = 1; j < 63; j += 2) {
-                h0 = max3(h0, s[j], s[j + 1]);
-                h1 = max3(h1, s[64 + j], s[64 + j + 1]);
+            for (int sb = 0; sb < 2; ++sb) {
+                const float* q = s + 64 * sb;
+                float a0 = q[0], a1 = q[1], a2 = q[2], a3 = q[3];
+                #pragma unroll
+                for (int j = 4; j + 8 <= 64; j += 8) {
+                    a0 = max3(a0, q[j + 0], q[j + 4]);
+                    a1 = max3(a1, q[j + 1], q[j + 5]);
+                    a2 = max3(a2, q[j + 2], q[j + 6]);
+                    a3 = max3(a3, q[j + 3], q[j + 7]);
+                }
+                a0 = fmaxf(a0, q[60]);
+                a1 = fmaxf(a1, q[61]);
+                a2 = fmaxf(a2, q[62]);
+                a3 = fmaxf(a3, q[63]);
+                hs[sb] = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
             }
-            h0 = fmaxf(h0, s[63]);
-            h1 = fmaxf(h1, s[127]);
-            const float mb = fmaxf(h0, h1) * A1;
-            const bool upd = (i == 0) || (mb - m_run > C::TAU);
-            const float m_new = upd ? mb : m_run;
-            const float f = (i > 0 && upd) ? ex2(m_run - m_new) : 1.0f;
-            m_run = m_new;
+            // running max after block i-1 from the other warpgroup; when it is
+            // read here the other warpgroup cannot publish again (its next
+            // block needs this warpgroup's m_i), so the parity is unambiguous
+            float m_prev = -INFINITY;
+            if (i > 0) {
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(BAR(B_MR + (1 - wg)), ((i - 1) >> 1) & 1, abort_flag, 9));
+                if (!ok) break;
+                m_prev = mx[(1 - wg) * 128 + row];
+            }
+            const float mb = fmaxf(hs[0], hs[1]) * A1;
+            const bool upd = (i == 0) || (mb - m_prev > C::TAU);
+            const float m_i = upd ? mb : m_prev;
+            // slot wg is free: the other warpgroup read it before it published
+            // m_{i-1}, which this warpgroup has just consumed
+            mx[wg * 128 + row] = m_i;
+            mbar_arrive(BAR(B_MR + wg));
+            const float f = (i > 0 && upd) ? ex2(m_prev - m_i) : 1.0f;
+            // P_i and its scale factors reuse the slots of block i-2: PV_{i-2}
+            // must be complete (PV_{i-4} is, as QK_i was issued after PV_{i-3},
+            // so the parity is unambiguous)
+            if (i >= 2) {
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(BAR(B_OD + (i & 1)), ((i - 2) >> 1) & 1, abort_flag, 11));
+                if (!ok) break;
+                tc_fence_after();
+            }
+            const uint32_t t_p = t_row + (wg ? C::COL_P1 : C::COL_P0);
 
             if constexpr (FP8) {
-                uint32_t pw[32];
-                int o0 = 0, o1 = 0;
+                int o[2] = {0, 0};
                 if (args.block_scale) {
-                    const float g0 = floorf(m_run - h0 * A1), g1 = floorf(m_run - h1 * A1);
-                    o0 = g0 > 0.0f ? (g0 < (float)kOMax ? (int)g0 : kOMax) : 0;
-                    o1 = g1 > 0.0f ? (g1 < (float)kOMax ? (int)g1 : kOMax) : 0;
-                }
-                if (args.p_mode == 1) {
-                    const float b0 = (8.0f * (kSigma + 7.0f + (float)o0 - m_run) - kBeta) * (1.0f / 256.0f);
-                    const float b1 = (8.0f * (kSigma + 7.0f + (float)o1 - m_run) - kBeta) * (1.0f / 256.0f);
                     #pragma unroll
-                    for (int w = 0; w < 32; ++w) {
-                        const float bb = w < 16 ? b0 : b1;
-                        const uint32_t c0 = lean_word(s[4 * w + 0], a_lean, bb);
-                        const uint32_t c1 = lean_word(s[4 * w + 1], a_lean, bb);
-                        const uint32_t c2 = lean_word(s[4 * w + 2], a_lean, bb);
-                        const uint32_t c3 = lean_word(s[4 * w + 3], a_lean, bb);
-                        pw[w] = __byte_perm(__byte_perm(c0, c1, 0x0040), __byte_perm(c2, c3, 0x0040),
-                                            0x5410);
-                    }
-                } else {
-                    const float e0 = kSigma + (float)o0 - m_run, e1 = kSigma + (float)o1 - m_run;
-                    #pragma unroll
-                    for (int w = 0; w < 32; ++w) {
-                        const float ee = w < 16 ? e0 : e1;
-                        const float p0 = ex2(fmaf(s[4 * w + 0], A1, ee));
-                        const float p1 = ex2(fmaf(s[4 * w + 1], A1, ee));
-                        const float p2 = ex2(fmaf(s[4 * w + 2], A1, ee));
-                        const float p3 = ex2(fmaf(s[4 * w + 3], A1, ee));
-                        pw[w] = cvt_e4m3x2(p0, p1) | (cvt_e4m3x2(p2, p3) << 16);
+                    for (int sb = 0; sb < 2; ++sb) {
+                        const float gap = floorf(m_i - hs[sb] * A1);
+                        o[sb] = gap > 0.0f ? (gap < (float)kOMax ? (int)gap : kOMax) : 0;
                     }
                 }
-                tmem_st32(t_s, pw);
+                #pragma unroll
+                for (int sb = 0; sb < 2; ++sb) {
+                    const float* q = s + 64 * sb;
+                    uint32_t pw[16];
+                    if (args.p_mode == 1) {
+                        const float bb = (8.0f * (kSigma + 7.0f + (float)o[sb] - m_i) - kBeta) * (1.0f / 256.0f);
+                        #pragma unroll
+                        for (int w = 0; w < 16; ++w) {
+                            const uint32_t q0 = lean_word(q[4 * w + 0], a_lean, bb);
+                            const uint32_t q1 = lean_word(q[4 * w + 1], a_lean, bb);
+                            const uint32_t q2 = lean_word(q[4 * w + 2], a_lean, bb);
+                            const uint32_t q3 = lean_word(q[4 * w + 3], a_lean, bb);
+                            pw[w] = __byte_perm(__byte_perm(q0, q1, 0x0040),
+                                                __byte_perm(q2, q3, 0x0040), 0x5410);
+                        }
+                    } else {
+                        const float ee = kSigma + (float)o[sb] - m_i;
+                        #pragma unroll
+                        for (int w = 0; w < 16; ++w) {
+                            const float p0 = ex2(fmaf(q[4 * w + 0], A1, ee));
+                            const float p1 = ex2(fmaf(q[4 * w + 1], A1, ee));
+                            const float p2 = ex2(fmaf(q[4 * w + 2], A1, ee));
+                            const float p3 = ex2(fmaf(q[4 * w + 3], A1, ee));
+                            pw[w] = cvt_e4m3x2(p0, p1) | (cvt_e4m3x2(p2, p3) << 16);
+                        }
+                    }
+                    tmem_st<16>(t_p + 16 * sb, pw);
+                }
                 // UE8M0 scale 2^-o per 32 keys (byte kk = K step kk); the word is
                 // repeated over the slot's 4 columns so that it is found whether
                 // the MMA reads the scale of row r at column 0 of the slot or at
                 // column r / 32
-                const uint32_t sf0 = static_cast<uint32_t>(127 - o0), sf1 = static_cast<uint32_t>(127 - o1);
+                const uint32_t sf0 = static_cast<uint32_t>(127 - o[0]);
+                const uint32_t sf1 = static_cast<uint32_t>(127 - o[1]);
                 const uint32_t sfw = sf0 | (sf0 << 8) | (sf1 << 16) | (sf1 << 24);
-                tmem_st4(t_row + ((i & 1) ? C::COL_SFA1 : C::COL_SFA0), sfw, sfw, sfw, sfw);
+                tmem_st4(t_row + (wg ? C::COL_SFA1 : C::COL_SFA0), sfw, sfw, sfw, sfw);
             } else {
-                float ls = 0.0f;
-                uint32_t lo[32], hi[32];
                 #pragma unroll
-                for (int w = 0; w < 32; ++w) {
-                    const float p0 = ex2(fmaf(s[2 * w], A1, -m_run));
-                    const float p1 = ex2(fmaf(s[2 * w + 1], A1, -m_run));
-                    const float p2 = ex2(fmaf(s[64 + 2 * w], A1, -m_run));
-                    const float p3 = ex2(fmaf(s[64 + 2 * w + 1], A1, -m_run));
-                    ls += (p0 + p1) + (p2 + p3);
-                    lo[w] = cvt_bf16x2(p0, p1);
-                    hi[w] = cvt_bf16x2(p2, p3);
+                for (int half = 0; half < 2; ++half) {
+                    const float* q = s + 64 * half;
+                    float ls0 = 0.0f, ls1 = 0.0f;
+                    uint32_t pw[32];
+                    #pragma unroll
+                    for (int w = 0; w < 32; ++w) {
+                        const float p0 = ex2(fmaf(q[2 * w], A1, -m_i));
+                        const float p1 = ex2(fmaf(q[2 * w + 1], A1, -m_i));
+                        ls0 += p0;
+                        ls1 += p1;
+                        pw[w] = cvt_bf16x2(p0, p1);
+                    }
+                    // own partial sum, kept relative to the max of its last block
+                    const float g = (half == 0 && m_own != -INFINITY) ? ex2(m_own - m_i) : 1.0f;
+                    l_own = l_own * g + (ls0 + ls1);
+                    tmem_st<32>(t_p + 32 * half, pw);
                 }
-                l_run = l_run * f + ls;
-                tmem_st32(t_s, lo);
-                tmem_st32(t_s + 32, hi);
+                m_own = m_i;
             }
-            // O (and L) must hold PV_{i-1} before a rescale and before PV_i
-            if (i > 0) {
-                ok = mbar_wait(BAR(B_OD), (i - 1) & 1, abort_flag, 7);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                tc_fence_after();
-                if (__any_sync(0xffffffffu, f != 1.0f)) {
+            if constexpr (FP8) m_own = m_i;
+            // A rescale of O (and L) needs PV_{i-1} complete; without one the
+            // warp goes on, since PV_i is ordered after PV_{i-1} anyway.
+            // PV_j arrives on o_done[j & 1]; here PV_{i-3} is complete (QK_i
+            // was issued after it) and PV_{i+1} cannot be issued before PV_i,
+            // so the parity of the wanted phase is unambiguous.
+            if (i > 0 && __any_sync(0xffffffffu, f != 1.0f)) {
+                bool ok2 = mbar_wait(BAR(B_OD + ((i - 1) & 1)), ((i - 1) >> 1) & 1, abort_flag, 7);
+                ok2 = __all_sync(0xffffffffu, ok2);
+                if (ok2) {
+                    tc_fence_after();
                     #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t r[32];
@@ -413,7 +536,7 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         tmem_wait_ld();
                         #pragma unroll
                         for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
-                        tmem_st32(t_row + C::COL_O + c * 32, r);
+                        tmem_st<32>(t_row + C::COL_O + c * 32, r);
                     }
                     if constexpr (FP8) {
                         uint32_t lr;
@@ -425,31 +548,58 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(BAR(B_PF + (i & 1)));
+            mbar_arrive(BAR(B_PF + wg));
         }
         // ------------------------------------------------------------ epilogue
-        if (ok) {
-            ok = mbar_wait(BAR(B_OD), (nblk - 1) & 1, abort_flag, 8);
-            ok = __all_sync(0xffffffffu, ok);
+        // The warpgroup that took the last block waits for its PV (it has
+        // seen PV_{nblk-3} complete before writing P_{nblk-1}, so the parity
+        // is unambiguous) and tells the other one.
+        const int last = nblk - 1;
+        if ((last & 1) == wg) {
+            if (ok)
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(BAR(B_OD + (last & 1)), (last >> 1) & 1, abort_flag, 8));
+            mbar_arrive(BAR(B_FIN));
+        } else {
+            ok = __all_sync(0xffffffffu, mbar_wait(BAR(B_FIN), 0, abort_flag, 10)) && ok;
         }
-        if (ok) {
-            tc_fence_after();
-            float inv;
-            if constexpr (FP8) {
+        float inv = 0.0f;
+        if constexpr (FP8) {
+            if (ok) {
+                tc_fence_after();
                 uint32_t lr;
                 tmem_ld1(t_row + C::COL_L, lr);
                 tmem_wait_ld();
                 inv = dv / __uint_as_float(lr);
-            } else {
-                inv = 1.0f / l_run;
             }
+        } else {
+            // every MMA has completed: the Q tile is free for the exchange
+            float* xl = reinterpret_cast<float*>(smem + C::OFF_Q);   // [2][2][128]
+            xl[(wg * 2 + 0) * 128 + row] = l_own;
+            xl[(wg * 2 + 1) * 128 + row] = m_own;
+            ok = bar_and(1, C::NSM, ok);
+            if (ok) {
+                const float m_fin = xl[((last & 1) * 2 + 1) * 128 + row];
+                float lt = 0.0f;
+                #pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    const float lw = xl[(w * 2 + 0) * 128 + row];
+                    const float mw = xl[(w * 2 + 1) * 128 + row];
+                    lt += lw > 0.0f ? lw * ex2(mw - m_fin) : 0.0f;
+                }
+                inv = 1.0f / lt;
+            }
+        }
+        if (ok) {
+            tc_fence_after();
+            const int c0 = wg * 64;                          // each warpgroup stores 64 columns
             const size_t orow = (static_cast<size_t>(b) * args.N + static_cast<size_t>(qt) * C::BM + row) *
                                     args.Hq + h;
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + orow * C::DV);
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + orow * C::DV + c0);
             #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < 2; ++c) {
                 uint32_t r[32];
-                tmem_ld32(t_row + C::COL_O + c * 32, r);
+                tmem_ld32(t_row + C::COL_O + c0 + c * 32, r);
                 tmem_wait_ld();
                 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -465,7 +615,7 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         tc_fence_before();
     }
     __syncthreads();
-    if (warp == 5) {
+    if (warp == C::WARP_MMA) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
     }
