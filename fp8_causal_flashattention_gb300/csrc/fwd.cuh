@@ -171,14 +171,18 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // tile: longest query tiles first, heads of one KV group adjacent
+    // tile order: KV-group major (all query tiles that read one K/V head run
+    // together, so that head stays in L2), then longest tile first, then the
+    // group's query heads side by side
     const int T = args.N / C::BM;
-    const int BH = args.B * args.Hq;
-    const int qt = T - 1 - static_cast<int>(blockIdx.x) / BH;
-    const int bh = static_cast<int>(blockIdx.x) % BH;
-    const int b = bh / args.Hq;
-    const int h = bh % args.Hq;
-    const int g = h / (args.Hq / args.Hkv);
+    const int grp = args.Hq / args.Hkv;
+    const int per_group = T * grp;
+    const int bg = static_cast<int>(blockIdx.x) / per_group;     // b * Hkv + g
+    const int rem = static_cast<int>(blockIdx.x) % per_group;
+    const int qt = T - 1 - rem / grp;
+    const int b = bg / args.Hkv;
+    const int g = bg % args.Hkv;
+    const int h = g * grp + rem % grp;
     const int nblk = qt + 1;
 
     if (threadIdx.x == 0) {
