@@ -31,7 +31,7 @@ def test_full_config_sampled_rows(lib, name):
         got = P.gather_rows(out, wl, rows)
         del out
         torch.cuda.empty_cache()
-        res = P.errors(got, inp, mode, rows, extra=(mode == "lean"))
+        res = P.errors(got, inp, mode, rows, extra=True)
         print(name, mode, res, flush=True)
         assert P.passes(res, mode), (name, mode, res)
     if wl.kind == "activation":
