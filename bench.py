@@ -340,6 +340,40 @@ def extras(args, P, fp8_peak, bf16_peak):
     return res
 
 
+def run_sweep(args):
+    """Every workload x mode, device-timed; one JSON line each (for tables)."""
+    import torch
+    import fp8_causal_flashattention_gb300 as Z
+    from tests import parity as P
+    Z.load()
+    torch.cuda.set_device(0)
+    peaks, _ = measured_peaks()
+    stream = torch.cuda.current_stream()
+    for name in ("pr1", "d128", "mla", "gqa_act", "sweep_1k", "sweep_4k", "sweep_16k", "sweep_64k"):
+        wl = S.WORKLOADS[name]
+        for mode in ("lean", "exact", "bf16"):
+            inp = S.make_inputs(wl, fp8=mode != "bf16", bf16=mode == "bf16")
+            dev = P.to_device(inp, mode != "bf16")
+            steps = max(5, min(200, int(2e13 / wl.causal_flops)))
+            clk = ClockSampler(None)
+            clk.start()
+            ms = time_launches(lambda: P.gpu_run(inp, mode, dev), steps, 3, stream)
+            clocks = clk.stop()
+            tf = wl.causal_flops / (ms * 1e-3) / 1e12
+            peak = peaks["bf16_tflops"] * (1.0 if mode == "bf16" else FP8_OVER_BF16)
+            abytes = wl.B * wl.N * (wl.Hq * wl.d_qk + wl.Hkv * (wl.d_qk + wl.d_v)) * (
+                2 if mode == "bf16" else 1) + wl.B * wl.N * wl.Hq * wl.d_v * 2
+            hbm_roof = abytes / (ms * 1e-3) / 1e9
+            print(json.dumps({"workload": name, "mode": mode, "tflops": tf, "ms": ms,
+                              "frac_of_tensor_peak": tf / peak,
+                              "algorithmic_GBps": hbm_roof,
+                              "frac_of_hbm": hbm_roof / peaks["hbm_gbs"],
+                              "sm_mhz": clocks.get("sm_mhz"), "reasons": clocks.get("reasons")}),
+                  flush=True)
+            del dev, inp
+            torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -351,7 +385,12 @@ def main():
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every workload and mode (one JSON line each)")
     args = ap.parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     wl = S.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, wl)
