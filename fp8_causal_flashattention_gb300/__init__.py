@@ -28,8 +28,8 @@ ZYFA_ERR_TIMEOUT = -6
 ZYFA_P_EXACT = 0
 ZYFA_P_LEAN = 1
 
-EXPORTS = ("zyfa_fwd", "zyfa_fwd_bf16", "zyfa_status_string",
-           "zyfa_last_device_status", "zyfa_version")
+EXPORTS = ("zyfa_fwd", "zyfa_fwd_bf16", "zyfa_fwd_ex", "zyfa_fwd_bf16_ex",
+           "zyfa_status_string", "zyfa_last_device_status", "zyfa_version")
 
 _lib = None
 
@@ -55,6 +55,10 @@ def load():
     lib.zyfa_fwd.argtypes = [vp, vp, vp, vp, vp, vp, vp] + [ci] * 9 + [vp]
     lib.zyfa_fwd_bf16.restype = ci
     lib.zyfa_fwd_bf16.argtypes = [vp, vp, vp, vp] + [ci] * 7 + [vp]
+    lib.zyfa_fwd_ex.restype = ci
+    lib.zyfa_fwd_ex.argtypes = [vp] * 8 + [ci] * 9 + [vp]
+    lib.zyfa_fwd_bf16_ex.restype = ci
+    lib.zyfa_fwd_bf16_ex.argtypes = [vp] * 5 + [ci] * 7 + [vp]
     lib.zyfa_status_string.restype = ctypes.c_char_p
     lib.zyfa_status_string.argtypes = [ci]
     lib.zyfa_last_device_status.restype = ci
@@ -98,6 +102,20 @@ def zyfa_fwd_bf16(q, k, v, out, B, Hq, Hkv, N, d_qk, d_v, causal=1, stream=None)
                                 d_v, causal, _stream(stream))
 
 
+def zyfa_fwd_ex(q, k, v, descale_q, descale_k, descale_v, out, lse, B, Hq, Hkv, N, d_qk, d_v,
+                causal=1, p_mode=ZYFA_P_LEAN, block_scale=1, stream=None) -> int:
+    """``zyfa_fwd_ex`` of include/zyfa.h (``lse`` may be None)."""
+    return load().zyfa_fwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(descale_q), _ptr(descale_k),
+                              _ptr(descale_v), _ptr(out), _ptr(lse), B, Hq, Hkv, N, d_qk, d_v,
+                              causal, p_mode, block_scale, _stream(stream))
+
+
+def zyfa_fwd_bf16_ex(q, k, v, out, lse, B, Hq, Hkv, N, d_qk, d_v, causal=1, stream=None) -> int:
+    """``zyfa_fwd_bf16_ex`` of include/zyfa.h (``lse`` may be None)."""
+    return load().zyfa_fwd_bf16_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv,
+                                   N, d_qk, d_v, causal, _stream(stream))
+
+
 def zyfa_status_string(status: int) -> str:
     return load().zyfa_status_string(int(status)).decode()
 
@@ -119,28 +137,31 @@ def _shape(q, k, v):
 
 
 def attention_fp8(q, k, v, descale_q=None, descale_k=None, descale_v=None, *,
-                  p_mode=ZYFA_P_LEAN, block_scale=1, out=None, stream=None):
+                  p_mode=ZYFA_P_LEAN, block_scale=1, out=None, return_lse=False, stream=None):
     """Causal FP8 attention on e4m3 tensors (torch.float8_e4m3fn or uint8),
     BSHD; descales are 1-element float32 device tensors (or None for 1.0).
-    Returns the BF16 output [B, N, Hq, d_v]."""
+    Returns the BF16 output [B, N, Hq, d_v] (and the FP32 LSE [B, Hq, N]
+    when ``return_lse``)."""
     import torch
     B, N, Hq, Hkv, d_qk, d_v = _shape(q, k, v)
     if out is None:
         out = torch.empty((B, N, Hq, d_v), dtype=torch.bfloat16, device=q.device)
-    rc = zyfa_fwd(q, k, v, descale_q, descale_k, descale_v, out, B, Hq, Hkv, N, d_qk, d_v,
-                  1, p_mode, block_scale, stream)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if return_lse else None
+    rc = zyfa_fwd_ex(q, k, v, descale_q, descale_k, descale_v, out, lse, B, Hq, Hkv, N, d_qk, d_v,
+                     1, p_mode, block_scale, stream)
     if rc != ZYFA_OK:
-        raise ZyfaError(rc, "zyfa_fwd")
-    return out
+        raise ZyfaError(rc, "zyfa_fwd_ex")
+    return (out, lse) if return_lse else out
 
 
-def attention_bf16(q, k, v, *, out=None, stream=None):
-    """Causal BF16 attention, BSHD.  Returns the BF16 output."""
+def attention_bf16(q, k, v, *, out=None, return_lse=False, stream=None):
+    """Causal BF16 attention, BSHD.  Returns the BF16 output (and the LSE)."""
     import torch
     B, N, Hq, Hkv, d_qk, d_v = _shape(q, k, v)
     if out is None:
         out = torch.empty((B, N, Hq, d_v), dtype=torch.bfloat16, device=q.device)
-    rc = zyfa_fwd_bf16(q, k, v, out, B, Hq, Hkv, N, d_qk, d_v, 1, stream)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if return_lse else None
+    rc = zyfa_fwd_bf16_ex(q, k, v, out, lse, B, Hq, Hkv, N, d_qk, d_v, 1, stream)
     if rc != ZYFA_OK:
-        raise ZyfaError(rc, "zyfa_fwd_bf16")
-    return out
+        raise ZyfaError(rc, "zyfa_fwd_bf16_ex")
+    return (out, lse) if return_lse else out

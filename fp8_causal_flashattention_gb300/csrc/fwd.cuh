@@ -45,6 +45,7 @@ constexpr int kOMax = 127;         // largest block exponent (UE8M0 2^-127)
 
 struct FwdArgs {
     void* out;                     // BF16 [B, N, Hq, 128]
+    float* lse;                    // FP32 [B, Hq, N] natural-log LSE, may be null
     const float* descale_q;        // device scalars, may be null (1.0)
     const float* descale_k;
     const float* descale_v;
@@ -568,13 +569,20 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             ok = __all_sync(0xffffffffu, mbar_wait(BAR(B_FIN), 0, abort_flag, 10)) && ok;
         }
         float inv = 0.0f;
+        const size_t lse_idx = (static_cast<size_t>(b) * args.Hq + h) * args.N +
+                               static_cast<size_t>(qt) * C::BM + row;
         if constexpr (FP8) {
             if (ok) {
                 tc_fence_after();
                 uint32_t lr;
                 tmem_ld1(t_row + C::COL_L, lr);
                 tmem_wait_ld();
-                inv = dv / __uint_as_float(lr);
+                const float l = __uint_as_float(lr);
+                inv = dv / l;
+                // LSE of the rounded weights: l is relative to the final
+                // running max and carries the 2^sigma shift (Sec. IV-B3)
+                if (args.lse && (last & 1) == wg)
+                    args.lse[lse_idx] = logf(l) + (m_own - kSigma) * 0.6931471805599453f;
             }
         } else {
             // every MMA has completed: the Q tile is free for the exchange
@@ -592,6 +600,7 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     lt += lw > 0.0f ? lw * ex2(mw - m_fin) : 0.0f;
                 }
                 inv = 1.0f / lt;
+                if (args.lse && wg == 0) args.lse[lse_idx] = logf(lt) + m_fin * 0.6931471805599453f;
             }
         }
         if (ok) {

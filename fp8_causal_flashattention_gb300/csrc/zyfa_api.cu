@@ -91,31 +91,47 @@ int launch(const void* q, const void* k, const void* v, const FwdArgs& a, cudaSt
 
 using namespace zyfa;
 
-extern "C" int zyfa_fwd(const void* q, const void* k, const void* v, const float* descale_q,
-                        const float* descale_k, const float* descale_v, void* out, int B, int Hq,
-                        int Hkv, int N, int d_qk, int d_v, int causal, int p_mode,
-                        int block_scale, void* stream) {
+extern "C" int zyfa_fwd_ex(const void* q, const void* k, const void* v, const float* descale_q,
+                           const float* descale_k, const float* descale_v, void* out, float* lse,
+                           int B, int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
+                           int p_mode, int block_scale, void* stream) {
     int rc = check_common(q, k, v, out, B, Hq, Hkv, N, d_qk, d_v, causal, 1);
     if (rc <= 0) return rc;
     if (p_mode != ZYFA_P_EXACT && p_mode != ZYFA_P_LEAN) return ZYFA_ERR_UNSUPPORTED;
     if (block_scale != 0 && block_scale != 1) return ZYFA_ERR_UNSUPPORTED;
-    if (!aligned(descale_q, 4) || !aligned(descale_k, 4) || !aligned(descale_v, 4))
+    if (!aligned(descale_q, 4) || !aligned(descale_k, 4) || !aligned(descale_v, 4) ||
+        !aligned(lse, 4))
         return ZYFA_ERR_ALIGN;
-    FwdArgs a{out, descale_q, descale_k, descale_v, B, Hq, Hkv, N, p_mode, block_scale,
+    FwdArgs a{out, lse, descale_q, descale_k, descale_v, B, Hq, Hkv, N, p_mode, block_scale,
               1.0f / sqrtf(static_cast<float>(d_qk))};
     auto s = static_cast<cudaStream_t>(stream);
     return d_qk == 128 ? launch<true, 128>(q, k, v, a, s) : launch<true, 192>(q, k, v, a, s);
 }
 
-extern "C" int zyfa_fwd_bf16(const void* q, const void* k, const void* v, void* out, int B,
-                             int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
-                             void* stream) {
+extern "C" int zyfa_fwd(const void* q, const void* k, const void* v, const float* descale_q,
+                        const float* descale_k, const float* descale_v, void* out, int B, int Hq,
+                        int Hkv, int N, int d_qk, int d_v, int causal, int p_mode,
+                        int block_scale, void* stream) {
+    return zyfa_fwd_ex(q, k, v, descale_q, descale_k, descale_v, out, nullptr, B, Hq, Hkv, N,
+                       d_qk, d_v, causal, p_mode, block_scale, stream);
+}
+
+extern "C" int zyfa_fwd_bf16_ex(const void* q, const void* k, const void* v, void* out,
+                                float* lse, int B, int Hq, int Hkv, int N, int d_qk, int d_v,
+                                int causal, void* stream) {
     int rc = check_common(q, k, v, out, B, Hq, Hkv, N, d_qk, d_v, causal, 2);
     if (rc <= 0) return rc;
-    FwdArgs a{out, nullptr, nullptr, nullptr, B, Hq, Hkv, N, 0, 0,
+    if (!aligned(lse, 4)) return ZYFA_ERR_ALIGN;
+    FwdArgs a{out, lse, nullptr, nullptr, nullptr, B, Hq, Hkv, N, 0, 0,
               1.0f / sqrtf(static_cast<float>(d_qk))};
     auto s = static_cast<cudaStream_t>(stream);
     return d_qk == 128 ? launch<false, 128>(q, k, v, a, s) : launch<false, 192>(q, k, v, a, s);
+}
+
+extern "C" int zyfa_fwd_bf16(const void* q, const void* k, const void* v, void* out, int B,
+                             int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
+                             void* stream) {
+    return zyfa_fwd_bf16_ex(q, k, v, out, nullptr, B, Hq, Hkv, N, d_qk, d_v, causal, stream);
 }
 
 extern "C" const char* zyfa_status_string(int status) {
@@ -150,4 +166,4 @@ extern "C" int zyfa_last_device_status(void* stream) {
     return ZYFA_OK;
 }
 
-extern "C" int zyfa_version(void) { return 100; }
+extern "C" int zyfa_version(void) { return 200; }

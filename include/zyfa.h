@@ -83,6 +83,30 @@ int zyfa_fwd_bf16(const void* q, const void* k, const void* v, void* out,
                   int B, int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
                   void* stream);
 
+/*
+ * zyfa_fwd with the log-sum-exp of each query row (NEXT to the forward pass:
+ * the paper's kernels return it so that results over different key ranges
+ * can be merged, Sec. IV-B3).
+ *   lse   NULL, or FP32 device memory [B, Hq, N] (4-byte aligned) that
+ *         receives ln(sum_j exp(c * dq * dk * q_i . k_j)) computed from the
+ *         same rounded, block-scaled probabilities the output is normalised
+ *         by: ln(l) + (m - 6) ln 2, l the rounded row sum relative to the
+ *         final running maximum m (base-2 units) and 6 the probability shift.
+ * Everything else as zyfa_fwd.
+ */
+int zyfa_fwd_ex(const void* q, const void* k, const void* v,
+                const float* descale_q, const float* descale_k, const float* descale_v,
+                void* out, float* lse, int B, int Hq, int Hkv, int N, int d_qk, int d_v,
+                int causal, int p_mode, int block_scale, void* stream);
+
+/*
+ * zyfa_fwd_bf16 with the log-sum-exp of each row, ln(l) + m ln 2 with l the
+ * FP32 row sum of the unrounded probabilities; lse as in zyfa_fwd_ex.
+ */
+int zyfa_fwd_bf16_ex(const void* q, const void* k, const void* v, void* out, float* lse,
+                     int B, int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
+                     void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* zyfa_status_string(int status);
 
