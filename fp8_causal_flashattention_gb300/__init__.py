@@ -29,7 +29,8 @@ ZYFA_P_EXACT = 0
 ZYFA_P_LEAN = 1
 
 EXPORTS = ("zyfa_fwd", "zyfa_fwd_bf16", "zyfa_fwd_ex", "zyfa_fwd_bf16_ex",
-           "zyfa_status_string", "zyfa_last_device_status", "zyfa_version")
+           "zyfa_status_string", "zyfa_last_device_status", "zyfa_selftest_timeout",
+           "zyfa_version")
 
 _lib = None
 
@@ -63,6 +64,8 @@ def load():
     lib.zyfa_status_string.argtypes = [ci]
     lib.zyfa_last_device_status.restype = ci
     lib.zyfa_last_device_status.argtypes = [vp]
+    lib.zyfa_selftest_timeout.restype = ci
+    lib.zyfa_selftest_timeout.argtypes = [vp]
     lib.zyfa_version.restype = ci
     lib.zyfa_version.argtypes = []
     _lib = lib
@@ -122,6 +125,10 @@ def zyfa_status_string(status: int) -> str:
 
 def zyfa_last_device_status(stream=None) -> int:
     return load().zyfa_last_device_status(_stream(stream))
+
+
+def zyfa_selftest_timeout(stream=None) -> int:
+    return load().zyfa_selftest_timeout(_stream(stream))
 
 
 def zyfa_version() -> int:

@@ -87,6 +87,21 @@ int launch(const void* q, const void* k, const void* v, const FwdArgs& a, cudaSt
 }
 
 }  // namespace
+
+// One thread waits on an mbarrier that nothing arrives at: the bounded wait
+// runs out, records the device status word and the kernel returns.
+__global__ void zyfa_selftest_wait_kernel() {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) (void)mbar_wait(smem_u32(&bar), 0, &abort_flag, 15);
+}
+
 }  // namespace zyfa
 
 using namespace zyfa;
@@ -164,6 +179,11 @@ extern "C" int zyfa_last_device_status(void* stream) {
         return ZYFA_ERR_TIMEOUT;
     }
     return ZYFA_OK;
+}
+
+extern "C" int zyfa_selftest_timeout(void* stream) {
+    zyfa_selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+    return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
 }
 
 extern "C" int zyfa_version(void) { return 200; }

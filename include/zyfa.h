@@ -118,6 +118,16 @@ const char* zyfa_status_string(int status);
  */
 int zyfa_last_device_status(void* stream);
 
+/*
+ * Test hook for the failure path (no counterpart in the paper): launches one
+ * thread that waits on an mbarrier nothing arrives at.  Its bounded wait
+ * runs out after about 1.5 s, records a timeout in the device status word
+ * and the kernel returns normally, so the next zyfa_last_device_status()
+ * on this device reports ZYFA_ERR_TIMEOUT and the context stays usable.
+ * Asynchronous on `stream`; returns ZYFA_OK or ZYFA_ERR_CUDA.
+ */
+int zyfa_selftest_timeout(void* stream);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int zyfa_version(void);
 

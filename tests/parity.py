@@ -20,7 +20,6 @@ from __future__ import annotations
 
 import numpy as np
 
-import oracle
 import synthetic as S
 
 FP8_REL_L2 = 1e-2
@@ -65,7 +64,10 @@ def gather_rows(out, wl: S.Workload, rows) -> np.ndarray:
     return sel.float().cpu().numpy().astype(np.float64)
 
 
-def oracle_params(wl: S.Workload, inp: S.Inputs, mode: str, max_mode=oracle.MAX_RUNNING):
+def oracle_params(wl: S.Workload, inp: S.Inputs, mode: str, max_mode=None):
+    import oracle
+    if max_mode is None:
+        max_mode = oracle.MAX_RUNNING
     fp8 = mode != "bf16"
     kw = dict(dtype="e4m3" if fp8 else "bf16", B=wl.B, Hq=wl.Hq, Hkv=wl.Hkv, N=wl.N,
               d_qk=wl.d_qk, d_v=wl.d_v, max_mode=max_mode)
@@ -83,6 +85,7 @@ def qkv_for(inp: S.Inputs, mode: str):
 
 
 def errors(gpu_rows: np.ndarray, inp: S.Inputs, mode: str, rows, extra: bool = True) -> dict:
+    import oracle
     wl = inp.wl
     q, k, v = qkv_for(inp, mode)
     p = oracle_params(wl, inp, mode)
