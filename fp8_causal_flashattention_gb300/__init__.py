@@ -144,7 +144,8 @@ def _shape(q, k, v):
 
 
 def attention_fp8(q, k, v, descale_q=None, descale_k=None, descale_v=None, *,
-                  p_mode=ZYFA_P_LEAN, block_scale=1, out=None, return_lse=False, stream=None):
+                  p_mode=ZYFA_P_LEAN, block_scale=1, causal=1, out=None, return_lse=False,
+                  stream=None):
     """Causal FP8 attention on e4m3 tensors (torch.float8_e4m3fn or uint8),
     BSHD; descales are 1-element float32 device tensors (or None for 1.0).
     Returns the BF16 output [B, N, Hq, d_v] (and the FP32 LSE [B, Hq, N]
@@ -155,20 +156,20 @@ def attention_fp8(q, k, v, descale_q=None, descale_k=None, descale_v=None, *,
         out = torch.empty((B, N, Hq, d_v), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if return_lse else None
     rc = zyfa_fwd_ex(q, k, v, descale_q, descale_k, descale_v, out, lse, B, Hq, Hkv, N, d_qk, d_v,
-                     1, p_mode, block_scale, stream)
+                     causal, p_mode, block_scale, stream)
     if rc != ZYFA_OK:
         raise ZyfaError(rc, "zyfa_fwd_ex")
     return (out, lse) if return_lse else out
 
 
-def attention_bf16(q, k, v, *, out=None, return_lse=False, stream=None):
+def attention_bf16(q, k, v, *, causal=1, out=None, return_lse=False, stream=None):
     """Causal BF16 attention, BSHD.  Returns the BF16 output (and the LSE)."""
     import torch
     B, N, Hq, Hkv, d_qk, d_v = _shape(q, k, v)
     if out is None:
         out = torch.empty((B, N, Hq, d_v), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if return_lse else None
-    rc = zyfa_fwd_bf16_ex(q, k, v, out, lse, B, Hq, Hkv, N, d_qk, d_v, 1, stream)
+    rc = zyfa_fwd_bf16_ex(q, k, v, out, lse, B, Hq, Hkv, N, d_qk, d_v, causal, stream)
     if rc != ZYFA_OK:
         raise ZyfaError(rc, "zyfa_fwd_bf16_ex")
     return (out, lse) if return_lse else out

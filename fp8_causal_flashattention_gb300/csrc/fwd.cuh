@@ -1,4 +1,4 @@
-// fwd.cuh -- causal attention forward (prefill) for sm_103a, FP8 e4m3 with
+// fwd.cuh -- attention forward (prefill, causal or not) for sm_103a, FP8 e4m3 with
 // Lean P / exact P, per-64-key power-of-two block scaling and division by the
 // sum of the rounded probabilities, plus the BF16 variant.
 //
@@ -52,6 +52,7 @@ struct FwdArgs {
     int B, Hq, Hkv, N;
     int p_mode;                    // 0 exact P, 1 Lean P
     int block_scale;               // 0 / 1
+    int causal;                    // 1: key j visible to query i iff j <= i; 0: all keys
     float softmax_scale;           // c
 };
 
@@ -184,7 +185,7 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int b = bg / args.Hkv;
     const int g = bg % args.Hkv;
     const int h = g * grp + rem % grp;
-    const int nblk = qt + 1;
+    const int nblk = args.causal ? qt + 1 : T;
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(B_QF), 1);
@@ -405,7 +406,7 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // S_i is in registers: QK_{i+2} may overwrite the buffer
             tc_fence_before();
             mbar_arrive(BAR(B_SX + wg));
-            if (i == nblk - 1) {                             // diagonal block: key > query
+            if (args.causal && i == nblk - 1) {             // diagonal block: key > query
                 #pragma unroll
                 for (int j = 0; j < 128; ++j)
                     if (j > row) s[j] = -INFINITY;

@@ -51,7 +51,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 int check_common(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
                  int N, int d_qk, int d_v, int causal, int esz) {
     if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0) return ZYFA_ERR_SHAPE;
-    if (causal != 1) return ZYFA_ERR_UNSUPPORTED;
+    if (causal != 0 && causal != 1) return ZYFA_ERR_UNSUPPORTED;
     if (!((d_qk == 128 || d_qk == 192) && d_v == 128)) return ZYFA_ERR_UNSUPPORTED;
     if (Hq % Hkv != 0) return ZYFA_ERR_SHAPE;
     if (N % 128 != 0) return ZYFA_ERR_SHAPE;
@@ -118,7 +118,7 @@ extern "C" int zyfa_fwd_ex(const void* q, const void* k, const void* v, const fl
         !aligned(lse, 4))
         return ZYFA_ERR_ALIGN;
     FwdArgs a{out, lse, descale_q, descale_k, descale_v, B, Hq, Hkv, N, p_mode, block_scale,
-              1.0f / sqrtf(static_cast<float>(d_qk))};
+              causal, 1.0f / sqrtf(static_cast<float>(d_qk))};
     auto s = static_cast<cudaStream_t>(stream);
     return d_qk == 128 ? launch<true, 128>(q, k, v, a, s) : launch<true, 192>(q, k, v, a, s);
 }
@@ -137,7 +137,7 @@ extern "C" int zyfa_fwd_bf16_ex(const void* q, const void* k, const void* v, voi
     int rc = check_common(q, k, v, out, B, Hq, Hkv, N, d_qk, d_v, causal, 2);
     if (rc <= 0) return rc;
     if (!aligned(lse, 4)) return ZYFA_ERR_ALIGN;
-    FwdArgs a{out, lse, nullptr, nullptr, nullptr, B, Hq, Hkv, N, 0, 0,
+    FwdArgs a{out, lse, nullptr, nullptr, nullptr, B, Hq, Hkv, N, 0, 0, causal,
               1.0f / sqrtf(static_cast<float>(d_qk))};
     auto s = static_cast<cudaStream_t>(stream);
     return d_qk == 128 ? launch<false, 128>(q, k, v, a, s) : launch<false, 192>(q, k, v, a, s);
@@ -154,7 +154,7 @@ extern "C" const char* zyfa_status_string(int status) {
         case ZYFA_OK: return "ok";
         case ZYFA_ERR_NULL: return "a required pointer is NULL";
         case ZYFA_ERR_SHAPE: return "invalid shape (sizes, Hq % Hkv, N % 128 or size limits)";
-        case ZYFA_ERR_UNSUPPORTED: return "unsupported configuration (causal, head dims or mode)";
+        case ZYFA_ERR_UNSUPPORTED: return "unsupported configuration (causal flag, head dims or mode)";
         case ZYFA_ERR_ALIGN: return "misaligned pointer (tensors need 16 bytes, scales 4)";
         case ZYFA_ERR_CUDA: return "CUDA launch or driver call failed";
         case ZYFA_ERR_TIMEOUT: return "a device-side wait ran out of time";

@@ -23,8 +23,9 @@
  *   - Layout: contiguous BSHD.  q [B, N, Hq, d_qk], k [B, N, Hkv, d_qk],
  *     v [B, N, Hkv, d_v], out [B, N, Hq, d_v].  Query head h reads key/value
  *     head h / (Hq / Hkv) (grouped-query attention, Table VI).
- *   - Supported: causal = 1; N a multiple of 128; (d_qk, d_v) = (128, 128)
- *     or (192, 128); Hq a multiple of Hkv.
+ *   - Supported: causal = 1 (the paper's setting) or 0 (every query sees
+ *     every key); N a multiple of 128; (d_qk, d_v) = (128, 128) or
+ *     (192, 128); Hq a multiple of Hkv.
  *   - Ownership: every buffer is device memory owned by the caller.  The
  *     library allocates no device memory per call, keeps no pointer after
  *     the call returns and writes nothing but `out`.
@@ -48,7 +49,7 @@ typedef enum {
     ZYFA_OK = 0,
     ZYFA_ERR_NULL = -1,         /* a required pointer is NULL                     */
     ZYFA_ERR_SHAPE = -2,        /* negative/zero sizes, Hq % Hkv, N % 128, limits */
-    ZYFA_ERR_UNSUPPORTED = -3,  /* causal != 1, head dims, p_mode / block_scale   */
+    ZYFA_ERR_UNSUPPORTED = -3,  /* causal not 0/1, head dims, p_mode / block_scale */
     ZYFA_ERR_ALIGN = -4,        /* a tensor not 16-byte aligned, a scale not 4    */
     ZYFA_ERR_CUDA = -5,         /* launch or driver call failed                   */
     ZYFA_ERR_TIMEOUT = -6       /* a device-side wait ran out (see below)         */

@@ -39,17 +39,18 @@ def to_device(inp: S.Inputs, fp8: bool = True):
     return t, None
 
 
-def gpu_run(inp: S.Inputs, mode: str, dev_tensors=None):
+def gpu_run(inp: S.Inputs, mode: str, dev_tensors=None, causal: int = 1):
     """mode: 'lean', 'exact', 'lean_nobs', 'exact_nobs' or 'bf16'.
     Returns the BF16 output as a torch tensor on the device."""
     import fp8_causal_flashattention_gb300 as Z
     fp8 = mode != "bf16"
     (q, k, v), ds = dev_tensors if dev_tensors is not None else to_device(inp, fp8)
     if not fp8:
-        return Z.attention_bf16(q, k, v)
+        return Z.attention_bf16(q, k, v, causal=causal)
     p_mode = Z.ZYFA_P_LEAN if mode.startswith("lean") else Z.ZYFA_P_EXACT
     bs = 0 if mode.endswith("nobs") else 1
-    return Z.attention_fp8(q, k, v, ds[0], ds[1], ds[2], p_mode=p_mode, block_scale=bs)
+    return Z.attention_fp8(q, k, v, ds[0], ds[1], ds[2], p_mode=p_mode, block_scale=bs,
+                           causal=causal)
 
 
 def gather_rows(out, wl: S.Workload, rows) -> np.ndarray:
@@ -64,13 +65,13 @@ def gather_rows(out, wl: S.Workload, rows) -> np.ndarray:
     return sel.float().cpu().numpy().astype(np.float64)
 
 
-def oracle_params(wl: S.Workload, inp: S.Inputs, mode: str, max_mode=None):
+def oracle_params(wl: S.Workload, inp: S.Inputs, mode: str, max_mode=None, causal: int = 1):
     import oracle
     if max_mode is None:
         max_mode = oracle.MAX_RUNNING
     fp8 = mode != "bf16"
     kw = dict(dtype="e4m3" if fp8 else "bf16", B=wl.B, Hq=wl.Hq, Hkv=wl.Hkv, N=wl.N,
-              d_qk=wl.d_qk, d_v=wl.d_v, max_mode=max_mode)
+              d_qk=wl.d_qk, d_v=wl.d_v, max_mode=max_mode, causal=causal)
     if fp8:
         kw.update(descale=inp.descale,
                   p_mode=oracle.P_LEAN if mode.startswith("lean") else oracle.P_EXACT,
@@ -84,11 +85,12 @@ def qkv_for(inp: S.Inputs, mode: str):
     return inp.q8, inp.k8, inp.v8
 
 
-def errors(gpu_rows: np.ndarray, inp: S.Inputs, mode: str, rows, extra: bool = True) -> dict:
+def errors(gpu_rows: np.ndarray, inp: S.Inputs, mode: str, rows, extra: bool = True,
+           causal: int = 1) -> dict:
     import oracle
     wl = inp.wl
     q, k, v = qkv_for(inp, mode)
-    p = oracle_params(wl, inp, mode)
+    p = oracle_params(wl, inp, mode, causal=causal)
     ref, ref_bf16, _ = oracle.fwd(p, q, k, v, rows)
     ref_b = oracle.bf16_bits_to_f64(ref_bf16)
     diff = gpu_rows - ref_b
@@ -105,7 +107,7 @@ def errors(gpu_rows: np.ndarray, inp: S.Inputs, mode: str, rows, extra: bool = T
         vmax = float(np.max(np.abs(oracle.e4m3_decode_table()[inp.v8]))) * inp.descale[2]
     res["max_abs_frac"] = res["max_abs"] / vmax
     if extra:
-        pe = oracle_params(wl, inp, mode, max_mode=oracle.MAX_EXACT)
+        pe = oracle_params(wl, inp, mode, max_mode=oracle.MAX_EXACT, causal=causal)
         refe, _, _ = oracle.fwd(pe, q, k, v, rows)
         ref64, _ = oracle.attn_fp64(p, q, k, v, rows)
         res["rel_l2_exactmax"] = float(np.linalg.norm(gpu_rows - refe) / np.linalg.norm(refe))

@@ -50,7 +50,8 @@ FAKE = 1 << 20          # 16-byte aligned, never dereferenced: checks fail first
     (dict(Hq=3, Hkv=2), Z.ZYFA_ERR_SHAPE),         # Hq % Hkv
     (dict(B=-1), Z.ZYFA_ERR_SHAPE),
     (dict(Hq=0), Z.ZYFA_ERR_SHAPE),
-    (dict(causal=0), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(causal=2), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(causal=-1), Z.ZYFA_ERR_UNSUPPORTED),
     (dict(d_qk=64), Z.ZYFA_ERR_UNSUPPORTED),
     (dict(d_v=192), Z.ZYFA_ERR_UNSUPPORTED),
     (dict(p_mode=2), Z.ZYFA_ERR_UNSUPPORTED),
