@@ -19,7 +19,11 @@ FlashAttention on AMD CDNA4"):
   Sec. IV-A "Lazy rescaling";
 * ``max_mode`` 0: the exact row maximum used to emulate the P term,
   Sec. V-E "Error of each stage of one call";
-* ``attn_fp64``: fp64 attention on the quantised inputs, Sec. V-D, fn. 15.
+* ``attn_fp64``: fp64 attention on the quantised inputs, Sec. V-D, fn. 15;
+* ``quantize`` (oracle/quantize.py): the quantisation pass before the
+  kernel -- K smoothing, the rotation R = diag(s)(C_m kron H_{D/m}) and the
+  per-tensor power-of-two descale, Sec. V-A "FP8 inputs and policies" and
+  "Rotation and K smoothing", Table XIII.
 
 Parity pins: see tests/test_oracle_*.py (brute force, printed constants,
 closed forms and invariants).  No function here is "parity unpinned".
@@ -98,6 +102,9 @@ def _load():
         lib.zo_e4m3_decode.argtypes = [ctypes.c_uint]
         lib.zo_e4m3_encode.restype = ctypes.c_uint
         lib.zo_e4m3_encode.argtypes = [ctypes.c_double]
+        lib.zo_e4m3_encode_n.restype = None
+        lib.zo_e4m3_encode_n.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_longlong]
         lib.zo_bf16_encode.restype = ctypes.c_uint
         lib.zo_bf16_encode.argtypes = [ctypes.c_double]
         lib.zo_bf16_decode.restype = ctypes.c_double
@@ -128,6 +135,14 @@ def e4m3_decode(code: int) -> float:
 
 def e4m3_encode(x: float) -> int:
     return int(_load().zo_e4m3_encode(float(x)))
+
+
+def e4m3_encode_array(x) -> np.ndarray:
+    """zo_e4m3_encode applied to every element of a float64 array."""
+    xa = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(xa.shape, dtype=np.uint8)
+    _load().zo_e4m3_encode_n(xa.ctypes.data, out.ctypes.data, xa.size)
+    return out
 
 
 def bf16_encode(x: float) -> int:

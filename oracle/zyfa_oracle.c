@@ -67,6 +67,7 @@ unsigned zo_e4m3_encode(double x)
     unsigned sign = signbit(x) ? 0x80u : 0u;
     double a = fabs(x);
     unsigned code;
+    if (isinf(a)) return sign | 0x7Eu;            /* saturates like any a > 448 */
     if (a < ldexp(1.0, -6)) {
         /* subnormal range: value = n x 2^-9, code = n (n = 8 is 2^-6) */
         double n = nearbyint(a * 512.0);          /* ties to even */
@@ -85,6 +86,12 @@ unsigned zo_e4m3_encode(double x)
         }
     }
     return sign | code;
+}
+
+/* Element-wise zo_e4m3_encode over an array (the quantisation oracle). */
+void zo_e4m3_encode_n(const double* x, unsigned char* out, long long n)
+{
+    for (long long i = 0; i < n; ++i) out[i] = (unsigned char)zo_e4m3_encode(x[i]);
 }
 
 /* ------------------------------------------------------------------------ */

@@ -79,6 +79,19 @@ def normal(shape, seed: int, stream: int, threads: int | None = None) -> np.ndar
     return out[:total].reshape(shape)
 
 
+STREAM_SIGNS = 100
+
+
+def rotation_signs(D: int, seed: int = 0) -> np.ndarray:
+    """float32 vector of D random signs (+1/-1): sign j is the top bit of
+    SplitMix64 counter j of stream (seed, STREAM_SIGNS)."""
+    key = _key(seed, STREAM_SIGNS)
+    with np.errstate(over="ignore"):
+        c = np.arange(D, dtype=np.uint64)
+        u = _mix(key + (c + np.uint64(1)) * GAMMA)
+    return np.where((u >> np.uint64(63)) == 0, 1.0, -1.0).astype(np.float32)
+
+
 def quantize_e4m3(x: np.ndarray):
     """Per-tensor e4m3 quantisation: returns (codes uint8, descale float)."""
     import torch
@@ -110,7 +123,7 @@ class Workload:
     N: int
     d_qk: int
     d_v: int
-    kind: str = "gaussian"          # "gaussian", "activation" or "sink"
+    kind: str = "gaussian"          # "gaussian", "activation", "sink" or "kbias"
     note: str = ""
 
     @property
@@ -169,6 +182,8 @@ def fp32_qkv(wl: Workload, seed: int = SEED):
         q, k, meta = _activation_like(wl, q, k, seed)
     elif wl.kind == "sink":
         q, k, meta = _sink(wl, q, k)
+    elif wl.kind == "kbias":
+        k, meta = _kbias(wl, k, seed)
     return q, k, v, meta
 
 
@@ -278,3 +293,18 @@ def _sink(wl: Workload, q, k, gap: float = SINK_GAP):
     k[:, :, :, 0] = 0.0
     k[:, 0, :, 0] = np.float32(gap / (c * 4.0))
     return q, k, {"sink_gap": gap}
+
+
+# --------------------------------------------------------------------------
+# keys with a shared offset
+# --------------------------------------------------------------------------
+KBIAS_STREAM = 3
+KBIAS_SCALE = 4.0           # per-channel offset ~ N(0, KBIAS_SCALE^2)
+
+
+def _kbias(wl: Workload, k, seed: int):
+    """Every key of KV head g gets the same offset vector bias[b, g, :],
+    drawn from N(0, KBIAS_SCALE^2): the keys then have a large mean over the
+    sequence, which K smoothing removes."""
+    bias = normal((wl.B, 1, wl.Hkv, wl.d_qk), seed, KBIAS_STREAM) * np.float32(KBIAS_SCALE)
+    return k + bias, {"kbias_scale": KBIAS_SCALE}
