@@ -331,6 +331,54 @@ def extras(args, P, fp8_peak, bf16_peak):
         res[f"{name}_{mode}"] = {"tflops": tf, "ms": ms, "frac_of_peak": tf / peak}
         del dev, inp
         torch.cuda.empty_cache()
+    res.update(quant_extras(steps))
+    return res
+
+
+def quant_extras(steps):
+    """The quantisation pass before the kernel on the d=128 workload's BF16
+    Q, K, V (each 32 heads x 32K x 128): Q rotated, K rotated and smoothed,
+    V plain; with static scales (the fused pass of Sec. V-A) and with
+    per-call scales.  HBM-bound: GB/s = algorithmic bytes / device time,
+    algorithmic bytes per element = 2 (read) + 1 (write) + 2 for every
+    further full read the definition needs (the mean before K smoothing,
+    the maximum before a per-call scale)."""
+    import torch
+    import fp8_causal_flashattention_gb300 as Z
+    peaks, _ = measured_peaks()
+    hbm = peaks["hbm_gbs"]
+    wl = S.WORKLOADS["d128"]
+    q, k, v, _ = S.fp32_qkv(wl)
+    dev = [torch.from_numpy(S.to_bf16_bits(a).view(np.int16)).view(torch.bfloat16).cuda()
+           for a in (q, k, v)]
+    del q, k, v
+    signs = torch.from_numpy(S.rotation_signs(wl.d_qk)).cuda()
+    outs = [torch.empty(t.shape, dtype=torch.float8_e4m3fn, device="cuda") for t in dev]
+    ds = [torch.empty(1, dtype=torch.float32, device="cuda") for _ in dev]
+    stream = torch.cuda.current_stream()
+    n = dev[0].numel()
+    res = {}
+    for label, static in (("static", 2.0 ** -5), ("dynamic", None)):
+        plan = ((dev[0], signs, False), (dev[1], signs, True), (dev[2], None, False))
+
+        def step():
+            for (x, s, sm), o, d in zip(plan, outs, ds):
+                Z.quantize(x, s, smooth=sm, static_descale=static, out=o, descale_out=d)
+
+        ms = time_launches(step, steps, 3, stream)
+        extra = 1 + (0 if static else 3)        # K's mean pass; one max pass per tensor
+        nbytes = n * (3 * 3 + 2 * extra)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[f"quant_d128_qkv_{label}"] = {"ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm,
+                                          "bytes": nbytes}
+    # the quantise kernel alone: Q rotated, static scale, 3 bytes per element
+    ms = time_launches(lambda: Z.quantize(dev[0], signs, static_descale=2.0 ** -5, out=outs[0],
+                                          descale_out=ds[0]), steps, 3, stream)
+    gbs = 3 * n / (ms * 1e-3) / 1e9
+    res["quant_d128_q_rot_static"] = {"ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm,
+                                      "bytes": 3 * n}
+    del dev, outs
+    torch.cuda.empty_cache()
     return res
 
 

@@ -29,7 +29,7 @@ ZYFA_P_EXACT = 0
 ZYFA_P_LEAN = 1
 
 EXPORTS = ("zyfa_fwd", "zyfa_fwd_bf16", "zyfa_fwd_ex", "zyfa_fwd_bf16_ex",
-           "zyfa_status_string", "zyfa_last_device_status", "zyfa_selftest_timeout",
+           "zyfa_quantize", "zyfa_status_string", "zyfa_last_device_status", "zyfa_selftest_timeout",
            "zyfa_version")
 
 _lib = None
@@ -60,6 +60,8 @@ def load():
     lib.zyfa_fwd_ex.argtypes = [vp] * 8 + [ci] * 9 + [vp]
     lib.zyfa_fwd_bf16_ex.restype = ci
     lib.zyfa_fwd_bf16_ex.argtypes = [vp] * 5 + [ci] * 7 + [vp]
+    lib.zyfa_quantize.restype = ci
+    lib.zyfa_quantize.argtypes = [vp, vp, ci, ctypes.c_float, vp, vp, vp] + [ci] * 4 + [vp]
     lib.zyfa_status_string.restype = ctypes.c_char_p
     lib.zyfa_status_string.argtypes = [ci]
     lib.zyfa_last_device_status.restype = ci
@@ -119,6 +121,14 @@ def zyfa_fwd_bf16_ex(q, k, v, out, lse, B, Hq, Hkv, N, d_qk, d_v, causal=1, stre
                                    N, d_qk, d_v, causal, _stream(stream))
 
 
+def zyfa_quantize(x, signs, smooth, static_descale, out, descale_out, mean_out, B, N, H, D,
+                  stream=None) -> int:
+    """``zyfa_quantize`` of include/zyfa.h (``signs`` / ``mean_out`` may be None)."""
+    return load().zyfa_quantize(_ptr(x), _ptr(signs), int(smooth), float(static_descale),
+                                _ptr(out), _ptr(descale_out), _ptr(mean_out), B, N, H, D,
+                                _stream(stream))
+
+
 def zyfa_status_string(status: int) -> str:
     return load().zyfa_status_string(int(status)).decode()
 
@@ -173,3 +183,30 @@ def attention_bf16(q, k, v, *, causal=1, out=None, return_lse=False, stream=None
     if rc != ZYFA_OK:
         raise ZyfaError(rc, "zyfa_fwd_bf16_ex")
     return (out, lse) if return_lse else out
+
+
+def quantize(x, signs=None, *, smooth=False, static_descale=None, out=None, descale_out=None,
+             return_mean=False, stream=None):
+    """BF16 tensor [B, N, H, D] -> (e4m3 codes as torch.float8_e4m3fn, descale as a
+    1-element float32 device tensor[, mean [B, H, D] float32]).
+
+    ``signs``: None (no rotation) or a float32 device tensor of D signs, the s
+    of R = diag(s)(C_m kron H_{D/m}); ``smooth``: subtract each head's mean
+    over the sequence first; ``static_descale``: a power of two, or None for
+    a per-call scale from the maximum."""
+    import torch
+    if x.dim() != 4:
+        raise ValueError("x must be [B, N, H, D]")
+    B, N, H, D = x.shape
+    if out is None:
+        out = torch.empty((B, N, H, D), dtype=torch.float8_e4m3fn, device=x.device)
+    if descale_out is None:
+        descale_out = torch.empty(1, dtype=torch.float32, device=x.device)
+    mean = (torch.empty((B, H, D), dtype=torch.float32, device=x.device)
+            if return_mean else None)
+    rc = zyfa_quantize(x, signs, 1 if smooth else 0,
+                       0.0 if static_descale is None else static_descale, out, descale_out,
+                       mean, B, N, H, D, stream)
+    if rc != ZYFA_OK:
+        raise ZyfaError(rc, "zyfa_quantize")
+    return (out, descale_out, mean) if return_mean else (out, descale_out)

@@ -27,8 +27,10 @@
  *     every key); N a multiple of 128; (d_qk, d_v) = (128, 128) or
  *     (192, 128); Hq a multiple of Hkv.
  *   - Ownership: every buffer is device memory owned by the caller.  The
- *     library allocates no device memory per call, keeps no pointer after
- *     the call returns and writes nothing but `out`.
+ *     attention entry points allocate no device memory, keep no pointer
+ *     after the call returns and write nothing but `out` (and `lse`).
+ *     zyfa_quantize takes stream-ordered scratch (cudaMallocAsync /
+ *     cudaFreeAsync on `stream`) when it needs a per-call maximum or a mean.
  *   - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL is the
  *     legacy default stream) and the call returns without synchronising.
  *   - Errors: a bad argument returns a negative status before anything is
@@ -107,6 +109,49 @@ int zyfa_fwd_ex(const void* q, const void* k, const void* v,
 int zyfa_fwd_bf16_ex(const void* q, const void* k, const void* v, void* out, float* lse,
                      int B, int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
                      void* stream);
+
+/*
+ * Quantisation pass before FP8 attention (Sec. V-A, "FP8 inputs and
+ * policies" and "Rotation and K smoothing"; Table XIII): BF16 -> e4m3 with
+ * one power-of-two scale per tensor, computed after the optional transforms.
+ * For each row x of D channels (row (b, n, h) of a BSHD tensor):
+ *     u = x - mean_n(x[b, :, h, :])      if smooth (K smoothing), else x
+ *     y = u R,  R = diag(s) (C_m kron H_{D/m})   if signs != NULL, else u
+ *     code = e4m3(y / d), round to nearest even, saturating at +-448,
+ *            NaN -> 0x7F
+ * with H the normalised Sylvester-Hadamard matrix, C_m the orthonormal
+ * DCT-II of size m (m = 1 for D = 128, 3 for D = 192), the element index
+ * j = a*(D/m) + b of R's rows and columns split as (DCT index a, Hadamard
+ * index b), and all arithmetic in FP32.  Rotate Q and K with the same
+ * signs: (QR)(KR)^T = QK^T, so the attention output is unchanged up to
+ * rounding; V is not rotated.
+ *   x             BF16 [B, N, H, D], contiguous, 16-byte aligned.
+ *   signs         NULL (no rotation) or D FP32 values in device memory whose
+ *                 sign bits are the s of R (the paper draws them at random
+ *                 with seed 0; any fixed +-1 vector is a valid R).
+ *   smooth        1: subtract the mean over the N positions of each (b, h)
+ *                 pair, channel by channel, before the rotation; 0: no.
+ *   static_descale  > 0: the descale d, a power of two in [2^-126, 2^127]
+ *                 (a static, calibrated scale; larger values saturate);
+ *                 0: per call, d = the smallest power of two >= 2^-126 with
+ *                 max |y| <= 448 d over the finite y (d = 1 if none is
+ *                 nonzero).
+ *   out           e4m3 codes [B, N, H, D], 16-byte aligned.
+ *   descale_out   one FP32 in device memory (required): receives d, so it
+ *                 can be passed straight to zyfa_fwd as descale_q/k/v.
+ *   mean_out      NULL, or FP32 [B, H, D] device memory (16-byte aligned)
+ *                 that receives the subtracted means (smooth = 1 only).
+ *   D             128 or 192.
+ * Reductions are deterministic (fixed summation order; the maximum is
+ * order-free), so repeated calls give identical bytes.  An empty tensor
+ * (B, N or H = 0) only writes descale_out.  Errors: ZYFA_ERR_SHAPE
+ * (negative sizes, grid limits), ZYFA_ERR_UNSUPPORTED (D, smooth,
+ * static_descale), ZYFA_ERR_NULL, ZYFA_ERR_ALIGN, ZYFA_ERR_CUDA (scratch
+ * allocation or launch).  Asynchronous on `stream`.
+ */
+int zyfa_quantize(const void* x, const float* signs, int smooth, float static_descale,
+                  void* out, float* descale_out, float* mean_out,
+                  int B, int N, int H, int D, void* stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char* zyfa_status_string(int status);

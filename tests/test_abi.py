@@ -92,3 +92,31 @@ def test_empty_problem_is_ok_without_launch(lib, B, N):
     assert lib.zyfa_fwd(None, None, None, None, None, None, None, B, 4, 4, N, 128, 128,
                         1, 1, 1, None) == Z.ZYFA_OK
     assert lib.zyfa_fwd_bf16(None, None, None, None, B, 4, 4, N, 128, 128, 1, None) == Z.ZYFA_OK
+
+
+@pytest.mark.parametrize("args,want", [
+    (dict(D=64), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(D=256), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(smooth=2), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(static=3.0), Z.ZYFA_ERR_UNSUPPORTED),          # not a power of two
+    (dict(static=-2.0), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(static=2.0 ** -127), Z.ZYFA_ERR_UNSUPPORTED),  # below the FP32-normal floor
+    (dict(static=float("inf")), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(B=-1), Z.ZYFA_ERR_SHAPE),
+    (dict(H=-3), Z.ZYFA_ERR_SHAPE),
+    (dict(descale_out=0), Z.ZYFA_ERR_NULL),
+    (dict(x=0), Z.ZYFA_ERR_NULL),
+    (dict(out=0), Z.ZYFA_ERR_NULL),
+    (dict(x=FAKE + 8), Z.ZYFA_ERR_ALIGN),
+    (dict(out=FAKE + 4), Z.ZYFA_ERR_ALIGN),
+    (dict(signs=FAKE + 2), Z.ZYFA_ERR_ALIGN),
+    (dict(mean=FAKE + 4), Z.ZYFA_ERR_ALIGN),
+    (dict(descale_out=FAKE + 1), Z.ZYFA_ERR_ALIGN),
+])
+def test_quantize_argument_errors(lib, args, want):
+    a = dict(x=FAKE, signs=FAKE, smooth=1, static=0.0, out=FAKE, descale_out=FAKE, mean=None,
+             B=1, N=100, H=2, D=128)
+    a.update(args)
+    rc = Z.zyfa_quantize(a["x"], a["signs"], a["smooth"], a["static"], a["out"],
+                         a["descale_out"], a["mean"], a["B"], a["N"], a["H"], a["D"], 0)
+    assert rc == want

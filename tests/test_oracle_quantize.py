@@ -112,6 +112,8 @@ def test_descale_closed_form():
     assert OQ.descale_for(448.0 * (1 + 2 ** -40)) == 2.0
     assert OQ.descale_for(224.0) == 0.5
     assert OQ.descale_for(224.0 * (1 + 2 ** -40)) == 1.0
+    assert OQ.descale_for(2.0 ** -140) == 2.0 ** -126        # FP32-normal floor
+    assert OQ.descale_for(448.0 * 2.0 ** -126) == 2.0 ** -126
     rng = np.random.default_rng(0)
     for a in 10.0 ** rng.uniform(-30, 30, 2000):
         d = OQ.descale_for(a)
