@@ -25,11 +25,12 @@ ZYFA_ERR_UNSUPPORTED = -3
 ZYFA_ERR_ALIGN = -4
 ZYFA_ERR_CUDA = -5
 ZYFA_ERR_TIMEOUT = -6
+ZYFA_ERR_SCRATCH = -7
 ZYFA_P_EXACT = 0
 ZYFA_P_LEAN = 1
 
 EXPORTS = ("zyfa_fwd", "zyfa_fwd_bf16", "zyfa_fwd_ex", "zyfa_fwd_bf16_ex",
-           "zyfa_quantize", "zyfa_status_string", "zyfa_last_device_status", "zyfa_selftest_timeout",
+           "zyfa_quantize", "zyfa_quantize_noalloc", "zyfa_status_string", "zyfa_last_device_status", "zyfa_selftest_timeout",
            "zyfa_version")
 
 _lib = None
@@ -62,6 +63,8 @@ def load():
     lib.zyfa_fwd_bf16_ex.argtypes = [vp] * 5 + [ci] * 7 + [vp]
     lib.zyfa_quantize.restype = ci
     lib.zyfa_quantize.argtypes = [vp, vp, ci, ctypes.c_float, vp, vp, vp] + [ci] * 4 + [vp]
+    lib.zyfa_quantize_noalloc.restype = ci
+    lib.zyfa_quantize_noalloc.argtypes = lib.zyfa_quantize.argtypes
     lib.zyfa_status_string.restype = ctypes.c_char_p
     lib.zyfa_status_string.argtypes = [ci]
     lib.zyfa_last_device_status.restype = ci
@@ -127,6 +130,15 @@ def zyfa_quantize(x, signs, smooth, static_descale, out, descale_out, mean_out, 
     return load().zyfa_quantize(_ptr(x), _ptr(signs), int(smooth), float(static_descale),
                                 _ptr(out), _ptr(descale_out), _ptr(mean_out), B, N, H, D,
                                 _stream(stream))
+
+
+def zyfa_quantize_noalloc(x, signs, smooth, static_descale, out, descale_out, mean_out, B, N,
+                          H, D, stream=None) -> int:
+    """``zyfa_quantize_noalloc`` of include/zyfa.h: zyfa_quantize with its
+    scratch in the library's fixed device buffer (no device allocation)."""
+    return load().zyfa_quantize_noalloc(_ptr(x), _ptr(signs), int(smooth),
+                                        float(static_descale), _ptr(out), _ptr(descale_out),
+                                        _ptr(mean_out), B, N, H, D, _stream(stream))
 
 
 def zyfa_status_string(status: int) -> str:

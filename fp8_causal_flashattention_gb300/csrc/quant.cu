@@ -24,6 +24,7 @@
 #include <cmath>
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/zyfa.h"
 
@@ -678,5 +679,100 @@ extern "C" int zyfa_quantize(const void* x, const float* signs, int smooth, floa
         const cudaError_t f = cudaFreeAsync(scratch, s);
         if (e == cudaSuccess) e = f;
     }
+    return e == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// zyfa_quantize_noalloc: the same passes with scratch taken from a fixed
+// device array instead of cudaMallocAsync.  For callers that must not
+// allocate device memory once they are running: a serving process with a
+// fixed memory budget, or one whose device memory pool belongs to another
+// allocator that the library must not draw from.
+//
+// The array lives at file scope, one copy per device, 16 MiB.  Its address
+// is looked up once per device with cudaGetSymbolAddress; that first call on
+// a device may load the module, so it must not happen inside a stream
+// capture.  Only the per-call maximum word must start at zero; it is zeroed
+// on the stream (cudaMemsetAsync) before the maximum pass of every call, and
+// everything else in the array is written before it is read.  All calls on a
+// device share the array: two calls whose work overlaps in time (different
+// streams, or different host threads) race on it, so callers serialise them.
+// ---------------------------------------------------------------------------
+namespace zyfa_quant {
+
+constexpr size_t kNoAllocScratchBytes = size_t{16} << 20;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device (cached).
+char* noalloc_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return static_cast<char*>(addr[dev]);
+}
+
+}  // namespace zyfa_quant
+
+extern "C" int zyfa_quantize_noalloc(const void* x, const float* signs, int smooth,
+                                     float static_descale, void* out, float* descale_out,
+                                     float* mean_out, int B, int N, int H, int D, void* stream) {
+    if (B < 0 || N < 0 || H < 0) return ZYFA_ERR_SHAPE;
+    if (D != 128 && D != 192) return ZYFA_ERR_UNSUPPORTED;
+    if (smooth != 0 && smooth != 1) return ZYFA_ERR_UNSUPPORTED;
+    if (!(static_descale == 0.f || normal_pow2(static_descale))) return ZYFA_ERR_UNSUPPORTED;
+    if (!descale_out) return ZYFA_ERR_NULL;
+    if (!aligned(descale_out, 4) || !aligned(signs, 4) || !aligned(mean_out, 16))
+        return ZYFA_ERR_ALIGN;
+    auto s = static_cast<cudaStream_t>(stream);
+    const bool dynamic = static_descale == 0.f;
+    const long long rows = static_cast<long long>(B) * N * H;
+    if (rows == 0) {
+        set_value_kernel<<<1, 1, 0, s>>>(descale_out, dynamic ? 1.f : static_descale);
+        return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
+    }
+    if (!x || !out) return ZYFA_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(out, 16)) return ZYFA_ERR_ALIGN;
+    if (rows >= (1ll << 31) || static_cast<long long>(H) * D >= (1ll << 31)) return ZYFA_ERR_SHAPE;
+    const bool sm = smooth == 1;
+    SumArgs sa = sum_plan(static_cast<const uint16_t*>(x), nullptr, B, N, H, D);
+    if (sm && static_cast<long long>(B) * sa.npb * sa.nchunk >= (1ll << 31)) return ZYFA_ERR_SHAPE;
+    const size_t partial_floats = sm ? static_cast<size_t>(B) * sa.nchunk * sa.HD : 0;
+    const size_t mean_floats = (sm && !mean_out) ? static_cast<size_t>(B) * sa.HD : 0;
+
+    // the same layout as zyfa_quantize's scratch: maximum word, partial sums,
+    // mean (when not the caller's)
+    const size_t amax_bytes = 256;
+    const size_t bytes = amax_bytes + (partial_floats + mean_floats) * sizeof(float);
+    const bool need_scratch = dynamic || sm;
+    if (need_scratch && bytes > kNoAllocScratchBytes) return ZYFA_ERR_SCRATCH;
+    char* sp = need_scratch ? noalloc_scratch() : nullptr;
+    if (need_scratch && !sp) return ZYFA_ERR_CUDA;
+    sa.partial = sm ? reinterpret_cast<float*>(sp + amax_bytes) : nullptr;
+
+    QuantArgs a{};
+    a.x = static_cast<const uint16_t*>(x);
+    a.out = static_cast<uint8_t*>(out);
+    a.signs = signs;
+    a.amax_bits = need_scratch ? reinterpret_cast<unsigned*>(sp) : nullptr;
+    a.mean = sm ? (mean_out ? mean_out : sa.partial + partial_floats) : nullptr;
+    a.descale_out = descale_out;
+    a.static_descale = static_descale;
+    a.N = N;
+    a.H = H;
+    a.rows = static_cast<uint32_t>(rows);
+    a.NH = static_cast<uint32_t>(static_cast<long long>(N) * H);
+    constants(D, a);
+    const bool rot = signs != nullptr;
+    const cudaError_t e = D == 128 ? dispatch<128>(a, sa, B, rot, sm, dynamic, s)
+                                   : dispatch<192>(a, sa, B, rot, sm, dynamic, s);
     return e == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
 }

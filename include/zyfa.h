@@ -54,7 +54,8 @@ typedef enum {
     ZYFA_ERR_UNSUPPORTED = -3,  /* causal not 0/1, head dims, p_mode / block_scale */
     ZYFA_ERR_ALIGN = -4,        /* a tensor not 16-byte aligned, a scale not 4    */
     ZYFA_ERR_CUDA = -5,         /* launch or driver call failed                   */
-    ZYFA_ERR_TIMEOUT = -6       /* a device-side wait ran out (see below)         */
+    ZYFA_ERR_TIMEOUT = -6,      /* a device-side wait ran out (see below)         */
+    ZYFA_ERR_SCRATCH = -7       /* needs more than zyfa_quantize_noalloc's buffer */
 } zyfa_status;
 
 enum { ZYFA_P_EXACT = 0, ZYFA_P_LEAN = 1 };
@@ -152,6 +153,35 @@ int zyfa_fwd_bf16_ex(const void* q, const void* k, const void* v, void* out, flo
 int zyfa_quantize(const void* x, const float* signs, int smooth, float static_descale,
                   void* out, float* descale_out, float* mean_out,
                   int B, int N, int H, int D, void* stream);
+
+/*
+ * zyfa_quantize without any device allocation (no counterpart in the
+ * paper).  For callers that must not allocate device memory once running
+ * -- a serving process with a fixed memory budget, or one whose device
+ * memory pool is managed by another allocator -- the scratch that
+ * zyfa_quantize takes with cudaMallocAsync (the per-call maximum word, the
+ * partial sums of the mean key and, when mean_out is NULL, the mean) comes
+ * from a fixed 16 MiB array in device memory, one per device.  Same
+ * arguments, same kernels, same results bit for bit.
+ *   - Limit: a call that needs more than 16 MiB of scratch returns
+ *     ZYFA_ERR_SCRATCH before launching anything.  Static scales without
+ *     smoothing need none, a per-call scale 256 bytes.  Smoothing needs
+ *     4 x B x nchunk x H x D bytes of partial sums, the library choosing
+ *     nchunk = min(ceil(608 / (B x ceil(H x D / 4096))), ceil(N / 16)),
+ *     plus 4 x B x H x D for the mean when mean_out is NULL: about 10 MB
+ *     for B = 1, H = 32, D = 128, N = 32768.
+ *   - The first call on each device looks the array up with
+ *     cudaGetSymbolAddress, which may load the module: make it outside any
+ *     stream capture.
+ *   - The maximum word is zeroed on `stream` by every call that uses it;
+ *     the rest of the scratch is written before it is read.
+ *   - All calls on one device share the array: calls whose work overlaps in
+ *     time (other streams, other host threads) race and must be serialised
+ *     by the caller.
+ */
+int zyfa_quantize_noalloc(const void* x, const float* signs, int smooth, float static_descale,
+                          void* out, float* descale_out, float* mean_out,
+                          int B, int N, int H, int D, void* stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char* zyfa_status_string(int status);
