@@ -22,7 +22,8 @@ smoothing", with footnotes 17, 18 and 25, and Table XIII):
 3. Per-tensor power-of-two descale, computed after the transforms: per call
    ("dynamic"), the smallest power of two d with amax <= 448 d, where amax is
    the largest finite |value| of the transformed tensor (d = 1 when amax is
-   0); or static, a power of two given by the caller.
+   0; d is kept at or above 2^-126 so that d and 1/d are normal FP32
+   numbers); or static, a power of two given by the caller.
 4. Codes: e4m3 round-to-nearest-even of value / d, saturating to +-448 (so a
    static scale that the tensor outgrows clips it); NaN -> 0x7F.
 
@@ -90,17 +91,22 @@ def rotation(signs) -> np.ndarray:
     return s[:, None] * np.kron(dct2(m), hadamard(D // m))
 
 
+MIN_DESCALE_EXP = -126
+
+
 def descale_for(amax: float) -> float:
-    """Smallest power of two d with amax <= 448 d (1 when amax is 0)."""
+    """Smallest power of two d >= 2^-126 with amax <= 448 d (1 when amax is
+    0).  The floor keeps d and 1/d normal FP32 numbers (the descale is an
+    FP32 value, Sec. II-C); it matters only for amax below about 2^-117."""
     if not amax > 0.0:
         return 1.0
     e = math.frexp(amax)[1] - 1            # amax in [2^e, 2^(e+1))
     e -= 8                                 # 448 = 1.75 * 2^8
     while amax > E4M3_MAX * 2.0 ** e:
         e += 1
-    while e > -200 and amax <= E4M3_MAX * 2.0 ** (e - 1):
+    while e > MIN_DESCALE_EXP and amax <= E4M3_MAX * 2.0 ** (e - 1):
         e -= 1
-    return 2.0 ** e
+    return 2.0 ** max(e, MIN_DESCALE_EXP)
 
 
 def bf16_bits_to_f64(bits) -> np.ndarray:
@@ -151,8 +157,8 @@ def quantize(x_bits, signs=None, smooth: bool = False, static_descale=None,
 
     if static_descale is not None:
         d = float(static_descale)
-        if not is_pow2(d):
-            raise ValueError("a static descale must be a power of two")
+        if not (is_pow2(d) and 2.0 ** MIN_DESCALE_EXP <= d <= 2.0 ** 127):
+            raise ValueError("a static descale must be a power of two in [2^-126, 2^127]")
         amax = None
     else:
         amax = 0.0
