@@ -278,6 +278,19 @@ __device__ __forceinline__ void mma_ts_mx8_elect(uint32_t d, uint32_t a_tmem, ui
                  : "memory");
 }
 
+// D(tmem) (+)= (A(smem) x 2^sfa) * (B(smem) x 2^sfb), kind::mxf8f6f4 with
+// one UE8M0 scale per 32 elements of K.
+__device__ __forceinline__ void mma_ss_mx8_elect(uint32_t d, uint64_t a, uint64_t b,
+                                                 uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                                 uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+                 " [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+                 :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_expect_tx_elect(uint32_t bar, uint32_t bytes) {
     asm volatile("{\n\t.reg .pred e;\n\t.reg .b64 st;\n\telect.sync _|e, 0xffffffff;\n\t"
                  "@e mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}"

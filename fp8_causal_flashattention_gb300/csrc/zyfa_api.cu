@@ -9,6 +9,7 @@
 
 #include "../../include/zyfa.h"
 #include "fwd.cuh"
+#include "fwd2.cuh"
 
 namespace zyfa {
 namespace {
@@ -66,6 +67,28 @@ int check_common(const void* q, const void* k, const void* v, void* out, int B, 
     return 1;   // proceed
 }
 
+// Two query tiles per CTA (fwd2.cuh), FP8 only: BF16 keeps one tile per CTA
+// (fwd.cuh), whose P stays in TMEM over the scores.
+template <int DQK>
+int launch2(const void* q, const void* k, const void* v, const FwdArgs& a, cudaStream_t stream) {
+    using C = Fwd2Cfg<DQK>;
+    CUtensorMap tq, tk, tv;
+    const CUtensorMapSwizzle swz =
+        C::CB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!make_map(&tq, q, false, DQK, a.Hq, a.N, a.B, C::CB, swz)) return ZYFA_ERR_CUDA;
+    if (!make_map(&tk, k, false, DQK, a.Hkv, a.N, a.B, C::CB, swz)) return ZYFA_ERR_CUDA;
+    if (!make_map(&tv, v, false, C::DV, a.Hkv, a.N, a.B, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        return ZYFA_ERR_CUDA;
+    auto kern = zyfa_fwd2_kernel<DQK>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
+        cudaSuccess)
+        return ZYFA_ERR_CUDA;
+    const int T = a.N / C::BM;
+    const unsigned grid = static_cast<unsigned>(a.B) * a.Hq * ((T + 1) / 2);
+    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, a);
+    return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
+}
+
 template <bool FP8, int DQK>
 int launch(const void* q, const void* k, const void* v, const FwdArgs& a, cudaStream_t stream) {
     using C = FwdCfg<FP8, DQK>;
@@ -120,6 +143,10 @@ extern "C" int zyfa_fwd_ex(const void* q, const void* k, const void* v, const fl
     FwdArgs a{out, lse, descale_q, descale_k, descale_v, B, Hq, Hkv, N, p_mode, block_scale,
               causal, 1.0f / sqrtf(static_cast<float>(d_qk))};
     auto s = static_cast<cudaStream_t>(stream);
+    // Lean P: two query tiles per CTA (fwd2.cuh).  Exact P is bound by the
+    // ex2 unit, where one tile per CTA (fwd.cuh) measures faster.
+    if (p_mode == ZYFA_P_LEAN)
+        return d_qk == 128 ? launch2<128>(q, k, v, a, s) : launch2<192>(q, k, v, a, s);
     return d_qk == 128 ? launch<true, 128>(q, k, v, a, s) : launch<true, 192>(q, k, v, a, s);
 }
 
