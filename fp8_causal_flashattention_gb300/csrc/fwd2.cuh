@@ -15,7 +15,9 @@
 // columns, FP32), O_t (128), the row sum L_t (16) and the scale factors
 // SFA_t / SFB_t (4 each).  Two full 128-column score buffers next to two O
 // accumulators would leave no room for L and the scale factors, hence the
-// halves.  P_t goes to shared memory (A operand of an SS block-scaled MMA).
+// halves.  P_t goes to shared memory (A operand of an SS block-scaled MMA);
+// P and its scale factors are double-buffered, so block j's are written as
+// soon as they are computed (PV(j-2) is long complete).
 //
 // Warps 0-3: softmax of tile A, 4-7: tile B, 8 / 9: QK issuers of tiles A /
 // B (8 also owns TMEM), 10 / 11: PV issuers of tiles A / B (10 also issues
@@ -36,6 +38,17 @@
 
 namespace zyfa {
 
+// The rounding step of lean_word on a pair: (z0, z1) * 256 + 1.5 * 2^23 with
+// one packed FMA (each half rounds like the scalar FMA); the codes end up in
+// the low bytes of the returned words.
+__device__ __forceinline__ void lean_word2(float z0, float z1, uint32_t& w0, uint32_t& w1) {
+    asm("{\n\t.reg .b64 Z, K, C;\n\t"
+        "mov.b64 Z, {%2, %3};\n\tmov.b64 K, {%4, %4};\n\tmov.b64 C, {%5, %5};\n\t"
+        "fma.rn.f32x2 Z, Z, K, C;\n\tmov.b64 {%0, %1}, Z;\n\t}"
+        : "=r"(w0), "=r"(w1)
+        : "f"(z0), "f"(z1), "f"(256.0f), "f"(12582912.0f));
+}
+
 template <int DQK>
 struct Fwd2Cfg {
     static constexpr int NSM = 256;                 // two softmax warpgroups
@@ -53,7 +66,7 @@ struct Fwd2Cfg {
     static constexpr int K_BYTES = BN * DQK;
     static constexpr int V_BYTES = BN * DV;
     static constexpr int P_BYTES = BM * BN;         // one tile, K-major, 128-byte swizzle
-    static constexpr int NST = DQK == 128 ? 4 : 3;
+    static constexpr int NST = DQK == 128 ? 4 : 2;
     static constexpr int QK_STEPS = DQK / 32;       // 32 bytes of K per MMA
     static constexpr int PV_STEPS = BN / 32;
     static constexpr int ONES_BYTES = 2048;         // 16 x 128 e4m3 ones
@@ -61,7 +74,7 @@ struct Fwd2Cfg {
     static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
     static constexpr int OFF_V = OFF_K + NST * K_BYTES;
     static constexpr int OFF_P = OFF_V + NST * V_BYTES;
-    static constexpr int OFF_ONES = OFF_P + 2 * P_BYTES;
+    static constexpr int OFF_ONES = OFF_P + 4 * P_BYTES;   // [tile][slot]
     static constexpr int OFF_BAR = OFF_ONES + ONES_BYTES;
     // q_full, k_full[NST], v_full[NST], kv_empty[NST], s_full[2], s_free[2],
     // p_full[2], o_done[2], fin[2], mma_done[4]; then the TMEM slot and the
@@ -72,8 +85,8 @@ struct Fwd2Cfg {
     static __host__ __device__ constexpr uint32_t col_s(int t) { return 64u * t; }
     static __host__ __device__ constexpr uint32_t col_o(int t) { return 128u + 128u * t; }
     static __host__ __device__ constexpr uint32_t col_l(int t) { return 384u + 16u * t; }
-    static __host__ __device__ constexpr uint32_t col_sfa(int t) { return 416u + 8u * t; }
-    static __host__ __device__ constexpr uint32_t col_sfb(int t) { return 420u + 8u * t; }
+    static __host__ __device__ constexpr uint32_t col_sfa(int t, int slot) { return 416u + 16u * t + 4u * slot; }
+    static __host__ __device__ constexpr uint32_t col_sfb(int t) { return 424u + 16u * t; }
     static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -207,11 +220,12 @@ zyfa_fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int nbt = t ? nb1 : nb0;
         const uint64_t dv0 = smem_desc(sbase + C::OFF_V, 1024, 1024, kSwizzle128B);
         const uint64_t d10 = smem_desc(sbase + C::OFF_ONES, 16, 1024, kSwizzle128B);
-        const uint64_t dp = smem_desc(sbase + C::OFF_P + t * C::P_BYTES, 16, 1024, kSwizzle128B);
         auto issue_pv = [&](int i) {
             const int st = i % C::NST;
+            const uint64_t dp = smem_desc(sbase + C::OFF_P + (2 * t + (i & 1)) * C::P_BYTES, 16, 1024,
+                                          kSwizzle128B);
             const uint64_t dv = dv0 + static_cast<uint64_t>((st * C::V_BYTES) >> 4);
-            const uint32_t sfa = tmem + C::col_sfa(t);
+            const uint32_t sfa = tmem + C::col_sfa(t, i & 1);
             const uint32_t sfb = tmem + C::col_sfb(t);
             #pragma unroll
             for (int kk = 0; kk < C::PV_STEPS; ++kk) {
@@ -336,10 +350,12 @@ zyfa_fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 const float bb = (8.0f * (kSigma + 7.0f + (float)o - m) - kBeta) * (1.0f / 256.0f);
                 #pragma unroll
                 for (int w = 0; w < 16; ++w) {
-                    const uint32_t q0 = lean_word(q[4 * w + 0], a_lean, bb);
-                    const uint32_t q1 = lean_word(q[4 * w + 1], a_lean, bb);
-                    const uint32_t q2 = lean_word(q[4 * w + 2], a_lean, bb);
-                    const uint32_t q3 = lean_word(q[4 * w + 3], a_lean, bb);
+                    // saturating FMA per score, then the rounding FMA on pairs
+                    uint32_t q0, q1, q2, q3;
+                    lean_word2(fma_sat(q[4 * w + 0], a_lean, bb), fma_sat(q[4 * w + 1], a_lean, bb),
+                               q0, q1);
+                    lean_word2(fma_sat(q[4 * w + 2], a_lean, bb), fma_sat(q[4 * w + 3], a_lean, bb),
+                               q2, q3);
                     pw[w] = __byte_perm(__byte_perm(q0, q1, 0x0040), __byte_perm(q2, q3, 0x0040),
                                         0x5410);
                 }
@@ -401,7 +417,6 @@ zyfa_fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         };
         float hs0 = -INFINITY, hs1 = -INFINITY;
         if (nbt > 0) ok = load_half(0, 0, hs0);
-        uint8_t* prow = smem + C::OFF_P + t * C::P_BYTES + row * 128;
         for (int j = 0; ok && j < nbt; ++j) {
             if (!(ok = load_half(j, 1, hs1))) break;
             // lazy rule per row (Sec. IV-A): adopt the block maximum only when
@@ -415,18 +430,14 @@ zyfa_fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             uint32_t pw0[16], pw1[16];
             codes64(s, m_i, o0, pw0);
             codes64(s + 64, m_i, o1, pw1);
-            // half 0 of the next block, so that its second QK can start
-            // before P_j is published
+            // half 0 of the next block first, so that its second QK starts
+            // as early as possible
             if (j + 1 < nbt && !(ok = load_half(j + 1, 0, hs0))) break;
-            // PV(j-1) must be complete: it read P and the scale factors, and O /
-            // L are rescaled below
-            if (j > 0) {
-                if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(B_OD + t), (j - 1) & 1, abort_flag, 32))))
-                    break;
-                tc_fence_after();
-            }
-            // row of P: 16-byte chunk c (keys 16c..16c+15) at chunk position
-            // c ^ (row & 7) of the row's 128 bytes (128-byte swizzle)
+            // P_j and its scale factors into slot j & 1, free since PV(j-2)
+            // completed (waited for in block j-1).  Row of P: 16-byte chunk c
+            // (keys 16c..16c+15) at chunk position c ^ (row & 7) of the row's
+            // 128 bytes (128-byte swizzle).
+            uint8_t* prow = smem + C::OFF_P + (2 * t + (j & 1)) * C::P_BYTES + row * 128;
             #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
@@ -439,7 +450,14 @@ zyfa_fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const uint32_t sf0 = static_cast<uint32_t>(127 - o0);
             const uint32_t sf1 = static_cast<uint32_t>(127 - o1);
             const uint32_t sfw = sf0 | (sf0 << 8) | (sf1 << 16) | (sf1 << 24);
-            tmem_st4(t_row + C::col_sfa(t), sfw, sfw, sfw, sfw);
+            tmem_st4(t_row + C::col_sfa(t, j & 1), sfw, sfw, sfw, sfw);
+            // PV(j-1) must be complete before O / L are rescaled and before
+            // P_j is published (which keeps p_full one phase ahead at most)
+            if (j > 0) {
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(B_OD + t), (j - 1) & 1, abort_flag, 32))))
+                    break;
+                tc_fence_after();
+            }
             if (j > 0 && __any_sync(0xffffffffu, f != 1.0f)) {
                 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
