@@ -143,10 +143,11 @@ extern "C" int zyfa_fwd_ex(const void* q, const void* k, const void* v, const fl
     FwdArgs a{out, lse, descale_q, descale_k, descale_v, B, Hq, Hkv, N, p_mode, block_scale,
               causal, 1.0f / sqrtf(static_cast<float>(d_qk))};
     auto s = static_cast<cudaStream_t>(stream);
-    // Lean P: two query tiles per CTA (fwd2.cuh).  Exact P is bound by the
-    // ex2 unit, where one tile per CTA (fwd.cuh) measures faster.
-    if (p_mode == ZYFA_P_LEAN)
-        return d_qk == 128 ? launch2<128>(q, k, v, a, s) : launch2<192>(q, k, v, a, s);
+    // Lean P at d_qk = 128: two query tiles per CTA (fwd2.cuh).  Exact P is
+    // bound by the ex2 unit, and at d_qk = 192 two Q tiles and double-buffered
+    // P leave shared memory for two K/V stages only; there one tile per CTA
+    // (fwd.cuh) measures faster.
+    if (p_mode == ZYFA_P_LEAN && d_qk == 128) return launch2<128>(q, k, v, a, s);
     return d_qk == 128 ? launch<true, 128>(q, k, v, a, s) : launch<true, 192>(q, k, v, a, s);
 }
 
