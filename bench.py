@@ -332,6 +332,20 @@ def extras(args, P, fp8_peak, bf16_peak):
         res[f"{name}_{mode}"] = {"tflops": tf, "ms": ms, "frac_of_peak": tf / peak}
         del dev, inp
         torch.cuda.empty_cache()
+    # the BHSD layout (Table VI): the same kernels on strided TMA maps
+    import fp8_causal_flashattention_gb300 as Z
+    wl = S.WORKLOADS["d128"]
+    inp = S.make_inputs(wl)
+    (q, k, v), ds = P.to_device(inp)
+    qs, ks, vs = (t.transpose(1, 2).contiguous().transpose(1, 2) for t in (q, k, v))
+    del q, k, v, inp
+    out = torch.empty((wl.B, wl.Hq, wl.N, wl.d_v), dtype=torch.bfloat16, device="cuda").transpose(1, 2)
+    ms = time_launches(lambda: Z.attention_fp8(qs, ks, vs, ds[0], ds[1], ds[2], out=out), steps, 3,
+                       stream)
+    tf = wl.causal_flops / (ms * 1e-3) / 1e12
+    res["d128_lean_bhsd"] = {"tflops": tf, "ms": ms, "frac_of_peak": tf / fp8_peak}
+    del qs, ks, vs, out
+    torch.cuda.empty_cache()
     res.update(quant_extras(steps))
     return res
 

@@ -30,6 +30,7 @@ ZYFA_P_EXACT = 0
 ZYFA_P_LEAN = 1
 
 EXPORTS = ("zyfa_fwd", "zyfa_fwd_bf16", "zyfa_fwd_ex", "zyfa_fwd_bf16_ex",
+           "zyfa_fwd_strided", "zyfa_fwd_bf16_strided",
            "zyfa_quantize", "zyfa_quantize_noalloc", "zyfa_status_string", "zyfa_last_device_status", "zyfa_selftest_timeout",
            "zyfa_version")
 
@@ -61,6 +62,10 @@ def load():
     lib.zyfa_fwd_ex.argtypes = [vp] * 8 + [ci] * 9 + [vp]
     lib.zyfa_fwd_bf16_ex.restype = ci
     lib.zyfa_fwd_bf16_ex.argtypes = [vp] * 5 + [ci] * 7 + [vp]
+    lib.zyfa_fwd_strided.restype = ci
+    lib.zyfa_fwd_strided.argtypes = [vp] * 8 + [ci] * 9 + [vp, vp]
+    lib.zyfa_fwd_bf16_strided.restype = ci
+    lib.zyfa_fwd_bf16_strided.argtypes = [vp] * 5 + [ci] * 7 + [vp, vp]
     lib.zyfa_quantize.restype = ci
     lib.zyfa_quantize.argtypes = [vp, vp, ci, ctypes.c_float, vp, vp, vp] + [ci] * 4 + [vp]
     lib.zyfa_quantize_noalloc.restype = ci
@@ -141,6 +146,34 @@ def zyfa_quantize_noalloc(x, signs, smooth, static_descale, out, descale_out, me
                                         _ptr(mean_out), B, N, H, D, _stream(stream))
 
 
+def _strides_arg(strides):
+    """12 int64 element strides as a ctypes array (or None)."""
+    if strides is None:
+        return None
+    arr = (ctypes.c_longlong * 12)(*[int(x) for x in strides])
+    return ctypes.cast(arr, ctypes.c_void_p), arr
+
+
+def zyfa_fwd_strided(q, k, v, descale_q, descale_k, descale_v, out, lse, B, Hq, Hkv, N, d_qk,
+                     d_v, causal=1, p_mode=ZYFA_P_LEAN, block_scale=1, strides=None,
+                     stream=None) -> int:
+    """``zyfa_fwd_strided`` of include/zyfa.h; ``strides``: 12 element strides or None."""
+    sa = _strides_arg(strides)
+    return load().zyfa_fwd_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(descale_q), _ptr(descale_k),
+                                   _ptr(descale_v), _ptr(out), _ptr(lse), B, Hq, Hkv, N, d_qk,
+                                   d_v, causal, p_mode, block_scale,
+                                   None if sa is None else sa[0], _stream(stream))
+
+
+def zyfa_fwd_bf16_strided(q, k, v, out, lse, B, Hq, Hkv, N, d_qk, d_v, causal=1, strides=None,
+                          stream=None) -> int:
+    """``zyfa_fwd_bf16_strided`` of include/zyfa.h."""
+    sa = _strides_arg(strides)
+    return load().zyfa_fwd_bf16_strided(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq,
+                                        Hkv, N, d_qk, d_v, causal,
+                                        None if sa is None else sa[0], _stream(stream))
+
+
 def zyfa_status_string(status: int) -> str:
     return load().zyfa_status_string(int(status)).decode()
 
@@ -161,15 +194,31 @@ def zyfa_version() -> int:
 def _shape(q, k, v):
     B, N, Hq, d_qk = q.shape
     if k.shape[0] != B or k.shape[1] != N or v.shape[:3] != k.shape[:3] or k.shape[3] != d_qk:
-        raise ValueError("q, k, v must be BSHD with matching B, N, Hkv and d_qk")
+        raise ValueError("q, k, v must be [B, N, H, d] with matching B, N, Hkv and d_qk")
     return B, N, Hq, k.shape[2], d_qk, v.shape[3]
+
+
+def _layout(q, k, v, out):
+    """Element strides (b, n, h) of the four [B, N, H, d] tensors, or None when
+    all are contiguous BSHD.  The last dimension must be contiguous."""
+    ts = (q, k, v, out)
+    if all(t.is_contiguous() for t in ts):
+        return None
+    st = []
+    for t in ts:
+        if t.stride(3) != 1:
+            raise ValueError("the last (channel) dimension must be contiguous")
+        st += [t.stride(0), t.stride(1), t.stride(2)]
+    return st
 
 
 def attention_fp8(q, k, v, descale_q=None, descale_k=None, descale_v=None, *,
                   p_mode=ZYFA_P_LEAN, block_scale=1, causal=1, out=None, return_lse=False,
                   stream=None):
     """Causal FP8 attention on e4m3 tensors (torch.float8_e4m3fn or uint8),
-    BSHD; descales are 1-element float32 device tensors (or None for 1.0).
+    [B, N, H, d] with any strides (e.g. a BHSD tensor viewed with
+    ``.transpose(1, 2)``) and a contiguous last dimension; descales are
+    1-element float32 device tensors (or None for 1.0).
     Returns the BF16 output [B, N, Hq, d_v] (and the FP32 LSE [B, Hq, N]
     when ``return_lse``)."""
     import torch
@@ -177,10 +226,10 @@ def attention_fp8(q, k, v, descale_q=None, descale_k=None, descale_v=None, *,
     if out is None:
         out = torch.empty((B, N, Hq, d_v), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if return_lse else None
-    rc = zyfa_fwd_ex(q, k, v, descale_q, descale_k, descale_v, out, lse, B, Hq, Hkv, N, d_qk, d_v,
-                     causal, p_mode, block_scale, stream)
+    rc = zyfa_fwd_strided(q, k, v, descale_q, descale_k, descale_v, out, lse, B, Hq, Hkv, N, d_qk,
+                          d_v, causal, p_mode, block_scale, _layout(q, k, v, out), stream)
     if rc != ZYFA_OK:
-        raise ZyfaError(rc, "zyfa_fwd_ex")
+        raise ZyfaError(rc, "zyfa_fwd_strided")
     return (out, lse) if return_lse else out
 
 
@@ -191,9 +240,10 @@ def attention_bf16(q, k, v, *, causal=1, out=None, return_lse=False, stream=None
     if out is None:
         out = torch.empty((B, N, Hq, d_v), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if return_lse else None
-    rc = zyfa_fwd_bf16_ex(q, k, v, out, lse, B, Hq, Hkv, N, d_qk, d_v, causal, stream)
+    rc = zyfa_fwd_bf16_strided(q, k, v, out, lse, B, Hq, Hkv, N, d_qk, d_v, causal,
+                               _layout(q, k, v, out), stream)
     if rc != ZYFA_OK:
-        raise ZyfaError(rc, "zyfa_fwd_bf16_ex")
+        raise ZyfaError(rc, "zyfa_fwd_bf16_strided")
     return (out, lse) if return_lse else out
 
 

@@ -54,6 +54,7 @@ struct FwdArgs {
     int block_scale;               // 0 / 1
     int causal;                    // 1: key j visible to query i iff j <= i; 0: all keys
     float softmax_scale;           // c
+    long long o_sb, o_sn, o_sh;    // element strides of out per batch, position, head
 };
 
 template <bool FP8, int DQK>
@@ -607,9 +608,9 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (ok) {
             tc_fence_after();
             const int c0 = wg * 64;                          // each warpgroup stores 64 columns
-            const size_t orow = (static_cast<size_t>(b) * args.N + static_cast<size_t>(qt) * C::BM + row) *
-                                    args.Hq + h;
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + orow * C::DV + c0);
+            const long long orow = b * args.o_sb + (static_cast<long long>(qt) * C::BM + row) * args.o_sn +
+                                   h * args.o_sh;
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + orow + c0);
             #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 uint32_t r[32];

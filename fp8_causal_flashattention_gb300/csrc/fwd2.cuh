@@ -494,9 +494,9 @@ zyfa_fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                            static_cast<size_t>(qt) * C::BM + row;
                     args.lse[lse_idx] = logf(l) + (m_run - kSigma) * 0.6931471805599453f;
                 }
-                const size_t orow = (static_cast<size_t>(b) * args.N + static_cast<size_t>(qt) * C::BM + row) *
-                                        args.Hq + h;
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + orow * C::DV);
+                const long long orow = b * args.o_sb + (static_cast<long long>(qt) * C::BM + row) * args.o_sn +
+                                       h * args.o_sh;
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + orow);
                 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t r[32];

@@ -28,16 +28,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 4-D map over a BSHD tensor: dims (d, H, N, B), box (inner, 1, 128, 1).
+// Element strides of one tensor per batch, position and head (the channel
+// dimension is contiguous).
+struct Strides {
+    long long b, n, h;
+};
+
+// 4-D map over a [B, N, H, d] tensor with strides st: dims (d, H, N, B), box
+// (inner, 1, 128, 1).
 bool make_map(CUtensorMap* m, const void* base, bool bf16, int d, int H, int N, int B,
-              int box_inner, CUtensorMapSwizzle swz) {
+              const Strides& st, int box_inner, CUtensorMapSwizzle swz) {
     auto enc = encode_fn();
     if (!enc) return false;
     const uint64_t esz = bf16 ? 2 : 1;
     cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
                           static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
-    cuuint64_t strides[3] = {d * esz, static_cast<uint64_t>(H) * d * esz,
-                             static_cast<uint64_t>(N) * H * d * esz};
+    cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.h) * esz, static_cast<cuuint64_t>(st.n) * esz,
+                             static_cast<cuuint64_t>(st.b) * esz};
     cuuint32_t box[4] = {static_cast<cuuint32_t>(box_inner), 1, 128, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
@@ -45,6 +52,41 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, int d, int H, int N, 
                      CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// The four tensors' strides: from the caller (12 values) or contiguous BSHD.
+struct Layout4 {
+    Strides q, k, v, o;
+};
+
+Layout4 layout_of(const long long* st, int Hq, int Hkv, int N, int d_qk, int d_v) {
+    if (st) return {{st[0], st[1], st[2]}, {st[3], st[4], st[5]}, {st[6], st[7], st[8]},
+                    {st[9], st[10], st[11]}};
+    const long long n = N;
+    return {{n * Hq * d_qk, static_cast<long long>(Hq) * d_qk, d_qk},
+            {n * Hkv * d_qk, static_cast<long long>(Hkv) * d_qk, d_qk},
+            {n * Hkv * d_v, static_cast<long long>(Hkv) * d_v, d_v},
+            {n * Hq * d_v, static_cast<long long>(Hq) * d_v, d_v}};
+}
+
+// TMA needs byte strides that are positive multiples of 16 below 2^40; the
+// output rows are written 16 bytes at a time.
+int check_strides(const Layout4& L, int esz) {
+    const Strides* in[3] = {&L.q, &L.k, &L.v};
+    for (const Strides* s : in) {
+        const long long v[3] = {s->b, s->n, s->h};
+        for (long long x : v) {
+            if (x <= 0) return ZYFA_ERR_SHAPE;
+            if ((x * esz) % 16 != 0) return ZYFA_ERR_ALIGN;
+            if (x * esz >= (1ll << 40)) return ZYFA_ERR_SHAPE;
+        }
+    }
+    const long long o[3] = {L.o.b, L.o.n, L.o.h};
+    for (long long x : o) {
+        if (x <= 0) return ZYFA_ERR_SHAPE;
+        if ((x * 2) % 16 != 0) return ZYFA_ERR_ALIGN;
+    }
+    return ZYFA_OK;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -60,9 +102,8 @@ int check_common(const void* q, const void* k, const void* v, void* out, int B, 
     if (!q || !k || !v || !out) return ZYFA_ERR_NULL;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
         return ZYFA_ERR_ALIGN;
-    // TMA limits: global dims < 2^32, byte strides < 2^40; grid < 2^31
-    const uint64_t bstride = static_cast<uint64_t>(N) * Hq * d_qk * esz;
-    if (bstride >= (1ull << 40)) return ZYFA_ERR_SHAPE;
+    // grid < 2^31 (the TMA stride limits are checked with the layout)
+    (void)esz;
     if (static_cast<uint64_t>(B) * Hq * (N / 128) >= (1ull << 31)) return ZYFA_ERR_SHAPE;
     return 1;   // proceed
 }
@@ -70,14 +111,15 @@ int check_common(const void* q, const void* k, const void* v, void* out, int B, 
 // Two query tiles per CTA (fwd2.cuh), FP8 only: BF16 keeps one tile per CTA
 // (fwd.cuh), whose P stays in TMEM over the scores.
 template <int DQK>
-int launch2(const void* q, const void* k, const void* v, const FwdArgs& a, cudaStream_t stream) {
+int launch2(const void* q, const void* k, const void* v, const FwdArgs& a, const Layout4& L,
+            cudaStream_t stream) {
     using C = Fwd2Cfg<DQK>;
     CUtensorMap tq, tk, tv;
     const CUtensorMapSwizzle swz =
         C::CB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    if (!make_map(&tq, q, false, DQK, a.Hq, a.N, a.B, C::CB, swz)) return ZYFA_ERR_CUDA;
-    if (!make_map(&tk, k, false, DQK, a.Hkv, a.N, a.B, C::CB, swz)) return ZYFA_ERR_CUDA;
-    if (!make_map(&tv, v, false, C::DV, a.Hkv, a.N, a.B, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!make_map(&tq, q, false, DQK, a.Hq, a.N, a.B, L.q, C::CB, swz)) return ZYFA_ERR_CUDA;
+    if (!make_map(&tk, k, false, DQK, a.Hkv, a.N, a.B, L.k, C::CB, swz)) return ZYFA_ERR_CUDA;
+    if (!make_map(&tv, v, false, C::DV, a.Hkv, a.N, a.B, L.v, 128, CU_TENSOR_MAP_SWIZZLE_128B))
         return ZYFA_ERR_CUDA;
     auto kern = zyfa_fwd2_kernel<DQK>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
@@ -90,15 +132,16 @@ int launch2(const void* q, const void* k, const void* v, const FwdArgs& a, cudaS
 }
 
 template <bool FP8, int DQK>
-int launch(const void* q, const void* k, const void* v, const FwdArgs& a, cudaStream_t stream) {
+int launch(const void* q, const void* k, const void* v, const FwdArgs& a, const Layout4& L,
+           cudaStream_t stream) {
     using C = FwdCfg<FP8, DQK>;
     CUtensorMap tq, tk, tv;
     const CUtensorMapSwizzle swz =
         C::CB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     const int inner = C::CB / C::ESZ;
-    if (!make_map(&tq, q, !FP8, DQK, a.Hq, a.N, a.B, inner, swz)) return ZYFA_ERR_CUDA;
-    if (!make_map(&tk, k, !FP8, DQK, a.Hkv, a.N, a.B, inner, swz)) return ZYFA_ERR_CUDA;
-    if (!make_map(&tv, v, !FP8, C::DV, a.Hkv, a.N, a.B, 128 / C::ESZ, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!make_map(&tq, q, !FP8, DQK, a.Hq, a.N, a.B, L.q, inner, swz)) return ZYFA_ERR_CUDA;
+    if (!make_map(&tk, k, !FP8, DQK, a.Hkv, a.N, a.B, L.k, inner, swz)) return ZYFA_ERR_CUDA;
+    if (!make_map(&tv, v, !FP8, C::DV, a.Hkv, a.N, a.B, L.v, 128 / C::ESZ, CU_TENSOR_MAP_SWIZZLE_128B))
         return ZYFA_ERR_CUDA;
     auto kern = zyfa_fwd_kernel<FP8, DQK>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
@@ -129,10 +172,11 @@ __global__ void zyfa_selftest_wait_kernel() {
 
 using namespace zyfa;
 
-extern "C" int zyfa_fwd_ex(const void* q, const void* k, const void* v, const float* descale_q,
-                           const float* descale_k, const float* descale_v, void* out, float* lse,
-                           int B, int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
-                           int p_mode, int block_scale, void* stream) {
+extern "C" int zyfa_fwd_strided(const void* q, const void* k, const void* v,
+                                const float* descale_q, const float* descale_k,
+                                const float* descale_v, void* out, float* lse, int B, int Hq,
+                                int Hkv, int N, int d_qk, int d_v, int causal, int p_mode,
+                                int block_scale, const long long* strides, void* stream) {
     int rc = check_common(q, k, v, out, B, Hq, Hkv, N, d_qk, d_v, causal, 1);
     if (rc <= 0) return rc;
     if (p_mode != ZYFA_P_EXACT && p_mode != ZYFA_P_LEAN) return ZYFA_ERR_UNSUPPORTED;
@@ -140,15 +184,25 @@ extern "C" int zyfa_fwd_ex(const void* q, const void* k, const void* v, const fl
     if (!aligned(descale_q, 4) || !aligned(descale_k, 4) || !aligned(descale_v, 4) ||
         !aligned(lse, 4))
         return ZYFA_ERR_ALIGN;
+    const Layout4 L = layout_of(strides, Hq, Hkv, N, d_qk, d_v);
+    if ((rc = check_strides(L, 1)) != ZYFA_OK) return rc;
     FwdArgs a{out, lse, descale_q, descale_k, descale_v, B, Hq, Hkv, N, p_mode, block_scale,
-              causal, 1.0f / sqrtf(static_cast<float>(d_qk))};
+              causal, 1.0f / sqrtf(static_cast<float>(d_qk)), L.o.b, L.o.n, L.o.h};
     auto s = static_cast<cudaStream_t>(stream);
     // Lean P at d_qk = 128: two query tiles per CTA (fwd2.cuh).  Exact P is
     // bound by the ex2 unit, and at d_qk = 192 two Q tiles and double-buffered
     // P leave shared memory for two K/V stages only; there one tile per CTA
     // (fwd.cuh) measures faster.
-    if (p_mode == ZYFA_P_LEAN && d_qk == 128) return launch2<128>(q, k, v, a, s);
-    return d_qk == 128 ? launch<true, 128>(q, k, v, a, s) : launch<true, 192>(q, k, v, a, s);
+    if (p_mode == ZYFA_P_LEAN && d_qk == 128) return launch2<128>(q, k, v, a, L, s);
+    return d_qk == 128 ? launch<true, 128>(q, k, v, a, L, s) : launch<true, 192>(q, k, v, a, L, s);
+}
+
+extern "C" int zyfa_fwd_ex(const void* q, const void* k, const void* v, const float* descale_q,
+                           const float* descale_k, const float* descale_v, void* out, float* lse,
+                           int B, int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
+                           int p_mode, int block_scale, void* stream) {
+    return zyfa_fwd_strided(q, k, v, descale_q, descale_k, descale_v, out, lse, B, Hq, Hkv, N,
+                            d_qk, d_v, causal, p_mode, block_scale, nullptr, stream);
 }
 
 extern "C" int zyfa_fwd(const void* q, const void* k, const void* v, const float* descale_q,
@@ -159,16 +213,26 @@ extern "C" int zyfa_fwd(const void* q, const void* k, const void* v, const float
                        d_qk, d_v, causal, p_mode, block_scale, stream);
 }
 
-extern "C" int zyfa_fwd_bf16_ex(const void* q, const void* k, const void* v, void* out,
-                                float* lse, int B, int Hq, int Hkv, int N, int d_qk, int d_v,
-                                int causal, void* stream) {
+extern "C" int zyfa_fwd_bf16_strided(const void* q, const void* k, const void* v, void* out,
+                                     float* lse, int B, int Hq, int Hkv, int N, int d_qk,
+                                     int d_v, int causal, const long long* strides,
+                                     void* stream) {
     int rc = check_common(q, k, v, out, B, Hq, Hkv, N, d_qk, d_v, causal, 2);
     if (rc <= 0) return rc;
     if (!aligned(lse, 4)) return ZYFA_ERR_ALIGN;
+    const Layout4 L = layout_of(strides, Hq, Hkv, N, d_qk, d_v);
+    if ((rc = check_strides(L, 2)) != ZYFA_OK) return rc;
     FwdArgs a{out, lse, nullptr, nullptr, nullptr, B, Hq, Hkv, N, 0, 0, causal,
-              1.0f / sqrtf(static_cast<float>(d_qk))};
+              1.0f / sqrtf(static_cast<float>(d_qk)), L.o.b, L.o.n, L.o.h};
     auto s = static_cast<cudaStream_t>(stream);
-    return d_qk == 128 ? launch<false, 128>(q, k, v, a, s) : launch<false, 192>(q, k, v, a, s);
+    return d_qk == 128 ? launch<false, 128>(q, k, v, a, L, s) : launch<false, 192>(q, k, v, a, L, s);
+}
+
+extern "C" int zyfa_fwd_bf16_ex(const void* q, const void* k, const void* v, void* out,
+                                float* lse, int B, int Hq, int Hkv, int N, int d_qk, int d_v,
+                                int causal, void* stream) {
+    return zyfa_fwd_bf16_strided(q, k, v, out, lse, B, Hq, Hkv, N, d_qk, d_v, causal, nullptr,
+                                 stream);
 }
 
 extern "C" int zyfa_fwd_bf16(const void* q, const void* k, const void* v, void* out, int B,

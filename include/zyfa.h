@@ -22,7 +22,8 @@
  * Common conventions
  *   - Layout: contiguous BSHD.  q [B, N, Hq, d_qk], k [B, N, Hkv, d_qk],
  *     v [B, N, Hkv, d_v], out [B, N, Hq, d_v].  Query head h reads key/value
- *     head h / (Hq / Hkv) (grouped-query attention, Table VI).
+ *     head h / (Hq / Hkv) (grouped-query attention, Table VI).  The
+ *     *_strided entry points take any strides (BHSD among them).
  *   - Supported: causal = 1 (the paper's setting) or 0 (every query sees
  *     every key); N a multiple of 128; (d_qk, d_v) = (128, 128) or
  *     (192, 128); Hq a multiple of Hkv.
@@ -182,6 +183,30 @@ int zyfa_quantize(const void* x, const float* signs, int smooth, float static_de
 int zyfa_quantize_noalloc(const void* x, const float* signs, int smooth, float static_descale,
                           void* out, float* descale_out, float* mean_out,
                           int B, int N, int H, int D, void* stream);
+
+/*
+ * zyfa_fwd_ex on tensors with any strides (Table VI runs both the BSHD and
+ * the BHSD layout).  Each tensor is addressed as [B, N, H, d] with a
+ * contiguous last dimension:
+ *   strides   NULL (contiguous BSHD, as zyfa_fwd_ex), or 12 element strides
+ *             {q_b, q_n, q_h, k_b, k_n, k_h, v_b, v_n, v_h, o_b, o_n, o_h}:
+ *             the distance between consecutive batches, positions and heads
+ *             of q, k, v and out.  BHSD is {H N d, d, N d} for each.
+ * Each stride must be positive; q, k and v strides times the element size
+ * must be multiples of 16 bytes (TMA) and below 2^40 bytes, out strides
+ * multiples of 8 elements.  ZYFA_ERR_SHAPE / ZYFA_ERR_ALIGN otherwise.
+ * Everything else as zyfa_fwd_ex (lse stays [B, Hq, N] contiguous).
+ */
+int zyfa_fwd_strided(const void* q, const void* k, const void* v,
+                     const float* descale_q, const float* descale_k, const float* descale_v,
+                     void* out, float* lse, int B, int Hq, int Hkv, int N, int d_qk, int d_v,
+                     int causal, int p_mode, int block_scale, const long long* strides,
+                     void* stream);
+
+/* zyfa_fwd_bf16_ex on strided tensors; strides as in zyfa_fwd_strided. */
+int zyfa_fwd_bf16_strided(const void* q, const void* k, const void* v, void* out, float* lse,
+                          int B, int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
+                          const long long* strides, void* stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char* zyfa_status_string(int status);

@@ -120,3 +120,24 @@ def test_quantize_argument_errors(lib, args, want):
     rc = Z.zyfa_quantize(a["x"], a["signs"], a["smooth"], a["static"], a["out"],
                          a["descale_out"], a["mean"], a["B"], a["N"], a["H"], a["D"], 0)
     assert rc == want
+
+
+def _bshd(B, N, H, d):
+    return [N * H * d, H * d, d]
+
+
+@pytest.mark.parametrize("which,bad,want", [
+    ("q", [4096 * 2 * 128, 2 * 128, 120], Z.ZYFA_ERR_ALIGN),     # head stride 120 B
+    ("k", [-1, 128, 128], Z.ZYFA_ERR_SHAPE),
+    ("v", [0, 128, 128], Z.ZYFA_ERR_SHAPE),
+    ("o", [256 * 2 * 128, 2 * 128, 124], Z.ZYFA_ERR_ALIGN),     # 248 B: not 16-byte aligned
+    ("q", [1 << 40, 256, 128], Z.ZYFA_ERR_SHAPE),                # byte stride >= 2^40
+])
+def test_strided_argument_errors(lib, which, bad, want):
+    st = {"q": _bshd(1, 256, 2, 128), "k": _bshd(1, 256, 1, 128), "v": _bshd(1, 256, 1, 128),
+          "o": [256 * 2 * 128, 2 * 128, 128]}
+    st[which] = bad
+    flat = st["q"] + st["k"] + st["v"] + st["o"]
+    rc = Z.zyfa_fwd_strided(FAKE, FAKE, FAKE, None, None, None, FAKE, None, 1, 2, 1, 256, 128, 128,
+                            1, 1, 1, flat, 0)
+    assert rc == want
