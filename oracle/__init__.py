@@ -20,6 +20,10 @@ FlashAttention on AMD CDNA4"):
 * ``max_mode`` 0: the exact row maximum used to emulate the P term,
   Sec. V-E "Error of each stage of one call";
 * ``attn_fp64``: fp64 attention on the quantised inputs, Sec. V-D, fn. 15;
+* ``dtype='mixed'``: BF16 QK^T with the FP8 PV path, the variant the
+  conclusion recommends (keep QK^T in BF16, run only PV in FP8); read as the
+  e4m3 method (tau = 0.125, sigma = 6, block scaling, rounded denominator)
+  with scores from BF16 Q and K and no Q/K descale;
 * ``quantize`` (oracle/quantize.py): the quantisation pass before the
   kernel -- K smoothing, the rotation R = diag(s)(C_m kron H_{D/m}) and the
   per-tensor power-of-two descale, Sec. V-A "FP8 inputs and policies" and
@@ -178,8 +182,11 @@ def make_params(*, dtype: str, B: int, Hq: int, Hkv: int, N: int, d_qk: int,
                 max_mode: int = MAX_RUNNING, tau=None, kv_block: int = KV_BLOCK,
                 scale_block: int = SCALE_BLOCK, denom_mode=None, sigma=None,
                 beta: float = BETA, causal: int = 1, o_max: int = O_MAX) -> Params:
-    """Parameters with the method's defaults for ``dtype`` ('e4m3' or 'bf16')."""
-    fp8 = dtype == "e4m3"
+    """Parameters with the method's defaults for ``dtype``: 'e4m3', 'bf16', or
+    'mixed' (BF16 Q and K, e4m3 V: the FP8 probability path of the e4m3
+    kernels after a BF16 QK^T; Q and K carry no descale)."""
+    mixed = dtype == "mixed"
+    fp8 = dtype == "e4m3" or mixed
     if not fp8 and dtype != "bf16":
         raise ValueError(dtype)
     if softmax_scale is None:
@@ -193,7 +200,9 @@ def make_params(*, dtype: str, B: int, Hq: int, Hkv: int, N: int, d_qk: int,
     if not fp8:
         descale = (1.0, 1.0, 1.0)
         block_scale = 0
-    return Params(0 if fp8 else 1, B, Hq, Hkv, N, d_qk, d_v, int(causal),
+    if mixed:
+        descale = (1.0, 1.0, descale[2])
+    return Params(2 if mixed else (0 if fp8 else 1), B, Hq, Hkv, N, d_qk, d_v, int(causal),
                   float(descale[0]), float(descale[1]), float(descale[2]),
                   float(softmax_scale), int(p_mode), int(block_scale),
                   int(max_mode), float(tau), int(kv_block), int(scale_block),
@@ -201,10 +210,10 @@ def make_params(*, dtype: str, B: int, Hq: int, Hkv: int, N: int, d_qk: int,
 
 
 def _prep(p: Params, q, k, v, rows):
-    width = 1 if p.dtype == 0 else 2
-    want = np.uint8 if width == 1 else np.uint16
+    qk_t = np.uint8 if p.dtype == 0 else np.uint16
+    v_t = np.uint16 if p.dtype == 1 else np.uint8
     arrs = []
-    for a, h, d in ((q, p.Hq, p.d_qk), (k, p.Hkv, p.d_qk), (v, p.Hkv, p.d_v)):
+    for a, h, d, want in ((q, p.Hq, p.d_qk, qk_t), (k, p.Hkv, p.d_qk, qk_t), (v, p.Hkv, p.d_v, v_t)):
         a = np.ascontiguousarray(a)
         if a.dtype != want:
             a = a.view(want)

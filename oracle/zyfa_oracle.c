@@ -156,7 +156,8 @@ unsigned zo_exact_code(double u, double sigma)
 /* Forward pass                                                              */
 /* ------------------------------------------------------------------------ */
 typedef struct {
-    int dtype;            /* 0: e4m3 codes (1 byte);  1: bf16 bits (2 bytes)  */
+    int dtype;            /* 0: e4m3 codes (1 byte);  1: bf16 bits (2 bytes); */
+                          /* 2: bf16 Q and K, e4m3 V, FP8 probabilities      */
     int B, Hq, Hkv, N, d_qk, d_v;
     int causal;           /* 1: key j visible to query i iff j <= i           */
     double descale_q, descale_k, descale_v;   /* per-tensor scales (Sec. II-C) */
@@ -181,10 +182,23 @@ static void build_table(void)
     for (int i = 0; i < 256; ++i) e4m3_table[i] = zo_e4m3_decode((unsigned)i);
 }
 
-static inline double load_elem(const zo_params* p, const void* base, size_t idx)
+static inline double load_e4m3(const void* base, size_t idx)
 {
-    if (p->dtype == 0) return e4m3_table[((const uint8_t*)base)[idx]];
+    return e4m3_table[((const uint8_t*)base)[idx]];
+}
+static inline double load_bf16(const void* base, size_t idx)
+{
     return zo_bf16_decode(((const uint16_t*)base)[idx]);
+}
+/* Q and K elements: e4m3 in dtype 0, bf16 otherwise. */
+static inline double load_qk(const zo_params* p, const void* base, size_t idx)
+{
+    return p->dtype == 0 ? load_e4m3(base, idx) : load_bf16(base, idx);
+}
+/* V elements: bf16 in dtype 1, e4m3 otherwise. */
+static inline double load_v(const zo_params* p, const void* base, size_t idx)
+{
+    return p->dtype == 1 ? load_bf16(base, idx) : load_e4m3(base, idx);
 }
 
 /* Probability of one key given u = x + o: returns the rounded value used in
@@ -226,12 +240,12 @@ static int row_scores(const zo_params* p, const void* q, const void* k,
     int g = h / (Hq / p->Hkv);
     int nk = p->causal ? i + 1 : N;
     size_t qoff = (((size_t)b * N + i) * Hq + h) * (size_t)p->d_qk;
-    for (int d = 0; d < p->d_qk; ++d) qv[d] = load_elem(p, q, qoff + d);
+    for (int d = 0; d < p->d_qk; ++d) qv[d] = load_qk(p, q, qoff + d);
     double cst = p->softmax_scale * p->descale_q * p->descale_k * M_LOG2E;
     for (int j = 0; j < nk; ++j) {
         size_t koff = (((size_t)b * N + j) * p->Hkv + g) * (size_t)p->d_qk;
         double s = 0.0;
-        for (int d = 0; d < p->d_qk; ++d) s += qv[d] * load_elem(p, k, koff + d);
+        for (int d = 0; d < p->d_qk; ++d) s += qv[d] * load_qk(p, k, koff + d);
         t[j] = cst * s;
     }
     return nk;
@@ -241,7 +255,7 @@ static inline void add_value(const zo_params* p, const void* v, long long b,
                              int g, int j, double w, double* acc)
 {
     size_t voff = (((size_t)b * p->N + j) * p->Hkv + g) * (size_t)p->d_v;
-    for (int d = 0; d < p->d_v; ++d) acc[d] += w * load_elem(p, v, voff + d);
+    for (int d = 0; d < p->d_v; ++d) acc[d] += w * load_v(p, v, voff + d);
 }
 
 static inline double nanmax(double a, double b)

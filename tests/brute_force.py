@@ -101,11 +101,15 @@ def decode(a, dtype):
 def forward(q, k, v, *, dtype, descale, p_mode, block_scale, max_mode, tau,
             kv_block, scale_block, denom_mode, sigma, beta, softmax_scale,
             o_max=127):
-    """Full (B, N, Hq, d_v) output in float64, all rows, causal."""
+    """Full (B, N, Hq, d_v) output in float64, all rows, causal.  dtype
+    'mixed': BF16 Q and K, e4m3 V and e4m3 probabilities."""
     B, N, Hq, dqk = q.shape
     Hkv, dv_ = k.shape[2], v.shape[3]
     grp = Hq // Hkv
-    Q, K, V = decode(q, dtype), decode(k, dtype), decode(v, dtype)
+    qk_dtype = "bf16" if dtype == "mixed" else dtype
+    v_dtype = "e4m3" if dtype == "mixed" else dtype
+    Q, K, V = decode(q, qk_dtype), decode(k, qk_dtype), decode(v, v_dtype)
+    dtype = v_dtype
     dq, dk, dvs = descale
     out = np.zeros((B, N, Hq, dv_))
     for b in range(B):
@@ -148,7 +152,9 @@ def attention_fp64(q, k, v, *, dtype, descale, softmax_scale):
     B, N, Hq, _ = q.shape
     Hkv = k.shape[2]
     grp = Hq // Hkv
-    Q, K, V = decode(q, dtype), decode(k, dtype), decode(v, dtype)
+    qk_dtype = "bf16" if dtype == "mixed" else dtype
+    v_dtype = "e4m3" if dtype == "mixed" else dtype
+    Q, K, V = decode(q, qk_dtype), decode(k, qk_dtype), decode(v, v_dtype)
     dq, dk, dvs = descale
     out = np.zeros((B, N, Hq, v.shape[3]))
     mask = np.tril(np.ones((N, N), dtype=bool))

@@ -283,3 +283,50 @@ def test_lse_close_to_fp64(golden):
     _, ref = oracle.attn_fp64(p, inp.q8, inp.k8, inp.v8, rows)
     worst = np.max(np.abs(lse - ref))
     assert worst <= golden["lse_worst_row_nats"]["range"][1]
+
+
+# ---------------------------------------------------------------------------
+# 'mixed': BF16 Q and K, e4m3 V, FP8 probabilities
+# ---------------------------------------------------------------------------
+def _tiny_mixed(B, N, Hq, Hkv, dqk, dv, seed):
+    q = S.normal((B, N, Hq, dqk), seed, 0)
+    k = S.normal((B, N, Hkv, dqk), seed, 1)
+    v = S.normal((B, N, Hkv, dv), seed, 2)
+    v8, dvs = S.quantize_e4m3(v)
+    return S.to_bf16_bits(q), S.to_bf16_bits(k), v8, (1.0, 1.0, dvs)
+
+
+@pytest.mark.parametrize("p_mode,block_scale,max_mode",
+                         list(itertools.product([0, 1, 2], [0, 1], [0, 1])))
+def test_mixed_matches_brute_force(p_mode, block_scale, max_mode):
+    q, k, v, ds = _tiny_mixed(1, 150, 2, 1, 16, 8, seed=31)
+    p, out, _, _ = _run(q, k, v, ds, "mixed", p_mode=p_mode, block_scale=block_scale,
+                        max_mode=max_mode, kv_block=48, scale_block=64, tau=0.125)
+    assert p.dtype == 2 and p.descale_q == 1.0 and p.descale_k == 1.0
+    assert _rel(out, _brute(q, k, v, ds, p, "mixed")) < 1e-12
+
+
+def test_mixed_unrounded_equals_fp64_attention():
+    q, k, v, ds = _tiny_mixed(1, 200, 2, 1, 16, 16, seed=32)
+    p = oracle.make_params(dtype="mixed", B=1, Hq=2, Hkv=1, N=200, d_qk=16, d_v=16, descale=ds)
+    ref, _ = oracle.attn_fp64(p, q, k, v)
+    ref_np = bf.attention_fp64(q, k, v, dtype="mixed", descale=ds, softmax_scale=p.softmax_scale)
+    assert _rel(ref.reshape(1, 2, 200, 16).transpose(0, 2, 1, 3), ref_np) < 1e-13
+    p2 = oracle.make_params(dtype="mixed", B=1, Hq=2, Hkv=1, N=200, d_qk=16, d_v=16,
+                            descale=ds, p_mode=2)
+    out, _, _ = oracle.fwd(p2, q, k, v)
+    assert _rel(out, ref) < 1e-12
+
+
+@pytest.mark.parametrize("p_mode", [0, 1])
+def test_mixed_equals_e4m3_on_shared_values(p_mode):
+    """Q and K values that e4m3 and BF16 both hold exactly (e4m3 codes decoded
+    into BF16): the mixed path must equal the e4m3 path with unit Q/K
+    descales, since only the loads differ."""
+    q8, k8, v8, (_, _, dvs) = _tiny(1, 140, 2, 2, 16, 8, seed=33)
+    tab = oracle.e4m3_decode_table()
+    q16 = S.to_bf16_bits(tab[q8].astype(np.float32))
+    k16 = S.to_bf16_bits(tab[k8].astype(np.float32))
+    _, out8, _, _ = _run(q8, k8, v8, (1.0, 1.0, dvs), "e4m3", p_mode=p_mode)
+    _, outm, _, _ = _run(q16, k16, v8, (1.0, 1.0, dvs), "mixed", p_mode=p_mode)
+    assert np.array_equal(out8, outm)
