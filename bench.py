@@ -332,6 +332,24 @@ def extras(args, P, fp8_peak, bf16_peak):
         res[f"{name}_{mode}"] = {"tflops": tf, "ms": ms, "frac_of_peak": tf / peak}
         del dev, inp
         torch.cuda.empty_cache()
+    # BF16 QK^T with FP8 PV (the variant the paper's conclusion recommends)
+    import fp8_causal_flashattention_gb300 as Z
+    wl = S.WORKLOADS["d128"]
+    inp = S.make_inputs(wl, fp8=True, bf16=True)
+    q16 = torch.from_numpy(inp.q16.view(np.int16)).view(torch.bfloat16).cuda()
+    k16 = torch.from_numpy(inp.k16.view(np.int16)).view(torch.bfloat16).cuda()
+    v8 = torch.from_numpy(inp.v8).cuda()
+    dv = torch.tensor([inp.descale[2]], dtype=torch.float32, device="cuda")
+    out = torch.empty((wl.B, wl.N, wl.Hq, wl.d_v), dtype=torch.bfloat16, device="cuda")
+    ms = time_launches(lambda: Z.attention_bf16qk_fp8pv(q16, k16, v8, dv, out=out), steps, 3, stream)
+    tf = wl.causal_flops / (ms * 1e-3) / 1e12
+    # QK^T runs at the BF16 rate and PV at the FP8 rate: the peak of the mix
+    # is the harmonic combination of half the FLOPs at each
+    mix_peak = 1.0 / (0.5 / bf16_peak + 0.5 / fp8_peak)
+    res["d128_bf16qk_fp8pv_lean"] = {"tflops": tf, "ms": ms, "frac_of_peak": tf / mix_peak,
+                                     "peak": mix_peak}
+    del q16, k16, v8, out, inp
+    torch.cuda.empty_cache()
     # the BHSD layout (Table VI): the same kernels on strided TMA maps
     import fp8_causal_flashattention_gb300 as Z
     wl = S.WORKLOADS["d128"]

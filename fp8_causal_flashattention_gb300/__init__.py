@@ -30,7 +30,7 @@ ZYFA_P_EXACT = 0
 ZYFA_P_LEAN = 1
 
 EXPORTS = ("zyfa_fwd", "zyfa_fwd_bf16", "zyfa_fwd_ex", "zyfa_fwd_bf16_ex",
-           "zyfa_fwd_strided", "zyfa_fwd_bf16_strided",
+           "zyfa_fwd_strided", "zyfa_fwd_bf16_strided", "zyfa_fwd_bf16qk_fp8pv",
            "zyfa_quantize", "zyfa_quantize_noalloc", "zyfa_status_string", "zyfa_last_device_status", "zyfa_selftest_timeout",
            "zyfa_version")
 
@@ -66,6 +66,8 @@ def load():
     lib.zyfa_fwd_strided.argtypes = [vp] * 8 + [ci] * 9 + [vp, vp]
     lib.zyfa_fwd_bf16_strided.restype = ci
     lib.zyfa_fwd_bf16_strided.argtypes = [vp] * 5 + [ci] * 7 + [vp, vp]
+    lib.zyfa_fwd_bf16qk_fp8pv.restype = ci
+    lib.zyfa_fwd_bf16qk_fp8pv.argtypes = [vp] * 6 + [ci] * 9 + [vp, vp]
     lib.zyfa_quantize.restype = ci
     lib.zyfa_quantize.argtypes = [vp, vp, ci, ctypes.c_float, vp, vp, vp] + [ci] * 4 + [vp]
     lib.zyfa_quantize_noalloc.restype = ci
@@ -174,6 +176,16 @@ def zyfa_fwd_bf16_strided(q, k, v, out, lse, B, Hq, Hkv, N, d_qk, d_v, causal=1,
                                         None if sa is None else sa[0], _stream(stream))
 
 
+def zyfa_fwd_bf16qk_fp8pv(q, k, v, descale_v, out, lse, B, Hq, Hkv, N, d_qk, d_v, causal=1,
+                          p_mode=ZYFA_P_LEAN, block_scale=1, strides=None, stream=None) -> int:
+    """``zyfa_fwd_bf16qk_fp8pv`` of include/zyfa.h."""
+    sa = _strides_arg(strides)
+    return load().zyfa_fwd_bf16qk_fp8pv(_ptr(q), _ptr(k), _ptr(v), _ptr(descale_v), _ptr(out),
+                                        _ptr(lse), B, Hq, Hkv, N, d_qk, d_v, causal, p_mode,
+                                        block_scale, None if sa is None else sa[0],
+                                        _stream(stream))
+
+
 def zyfa_status_string(status: int) -> str:
     return load().zyfa_status_string(int(status)).decode()
 
@@ -272,3 +284,19 @@ def quantize(x, signs=None, *, smooth=False, static_descale=None, out=None, desc
     if rc != ZYFA_OK:
         raise ZyfaError(rc, "zyfa_quantize")
     return (out, descale_out, mean) if return_mean else (out, descale_out)
+
+
+def attention_bf16qk_fp8pv(q, k, v, descale_v=None, *, p_mode=ZYFA_P_LEAN, block_scale=1,
+                           causal=1, out=None, return_lse=False, stream=None):
+    """BF16 Q and K, e4m3 V (torch.float8_e4m3fn or uint8): BF16 QK^T, FP8
+    probabilities and PV.  Shapes and strides as attention_fp8."""
+    import torch
+    B, N, Hq, Hkv, d_qk, d_v = _shape(q, k, v)
+    if out is None:
+        out = torch.empty((B, N, Hq, d_v), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device) if return_lse else None
+    rc = zyfa_fwd_bf16qk_fp8pv(q, k, v, descale_v, out, lse, B, Hq, Hkv, N, d_qk, d_v, causal,
+                               p_mode, block_scale, _layout(q, k, v, out), stream)
+    if rc != ZYFA_OK:
+        raise ZyfaError(rc, "zyfa_fwd_bf16qk_fp8pv")
+    return (out, lse) if return_lse else out

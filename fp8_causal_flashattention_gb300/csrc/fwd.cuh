@@ -57,7 +57,9 @@ struct FwdArgs {
     long long o_sb, o_sn, o_sh;    // element strides of out per batch, position, head
 };
 
-template <bool FP8, int DQK>
+// FP8: e4m3 V and probabilities (the PV path); QK16: Q and K in BF16 (the
+// BF16 kernel has both; QK16 with FP8 is the BF16-QK^T / FP8-PV variant).
+template <bool FP8, int DQK, bool QK16 = !FP8>
 struct FwdCfg {
     // two softmax warpgroups; warpgroup w takes the key blocks i = w (mod 2)
     static constexpr int NWG = 2;
@@ -67,17 +69,19 @@ struct FwdCfg {
     static constexpr int BM = 128;            // query rows per tile
     static constexpr int BN = 128;            // keys per block
     static constexpr int DV = 128;
-    static constexpr int ESZ = FP8 ? 1 : 2;
-    static constexpr int CB = (FP8 && DQK == 192) ? 64 : 128;   // bytes per Q/K chunk row
+    static constexpr int ESZ = QK16 ? 2 : 1;                    // Q/K element bytes
+    static constexpr int VSZ = FP8 ? 1 : 2;                     // V (and P) element bytes
+    static constexpr int CB = (ESZ == 1 && DQK == 192) ? 64 : 128;   // bytes per Q/K chunk row
     static constexpr int NCH = DQK * ESZ / CB;                  // Q/K chunks
     static constexpr uint32_t SWZ = CB == 128 ? kSwizzle128B : kSwizzle64B;
-    static constexpr int VCH = DV * ESZ / 128;                  // V chunks of 128 bytes
+    static constexpr int VCH = DV * VSZ / 128;                  // V chunks of 128 bytes
     static constexpr int Q_BYTES = BM * DQK * ESZ;
     static constexpr int K_BYTES = BN * DQK * ESZ;
-    static constexpr int V_BYTES = BN * DV * ESZ;
-    static constexpr int NST = FP8 ? 4 : (DQK == 128 ? 3 : 2);  // K/V ring stages
+    static constexpr int V_BYTES = BN * DV * VSZ;
+    // K/V ring stages: as many as fit next to the Q tile (227 KB)
+    static constexpr int NST = (FP8 && !QK16) ? 4 : (DQK == 128 ? 3 : 2);
     static constexpr int QK_STEPS = DQK * ESZ / 32;             // 32 bytes of K per MMA
-    static constexpr int PV_STEPS = BN * ESZ / 32;
+    static constexpr int PV_STEPS = BN * VSZ / 32;
     static constexpr int ONES_BYTES = FP8 ? 2048 : 0;           // 16 x 128 e4m3 ones
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_BYTES;
@@ -151,11 +155,11 @@ __device__ __forceinline__ bool bar_and(int id, int nthreads, bool pred) {
     return r != 0;
 }
 
-template <bool FP8, int DQK>
-__global__ void __launch_bounds__(FwdCfg<FP8, DQK>::THREADS, 1)
+template <bool FP8, int DQK, bool QK16 = !FP8>
+__global__ void __launch_bounds__(FwdCfg<FP8, DQK, QK16>::THREADS, 1)
 zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
-    using C = FwdCfg<FP8, DQK>;
+    using C = FwdCfg<FP8, DQK, QK16>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
     if (sbase & 1023u) {   // swizzled TMA / MMA operands need 1 KB alignment
@@ -253,7 +257,7 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             #pragma unroll
             for (int c = 0; c < C::VCH; ++c)
                 tma_load_4d_elect(sbase + C::OFF_V + st * C::V_BYTES + c * (C::BN * 128), &tm_v,
-                                  BAR(B_VF + st), c * 128 / C::ESZ, g, i * C::BN, b);
+                                  BAR(B_VF + st), c * 128 / C::VSZ, g, i * C::BN, b);
             ++issued;
         }
         if (*abort_flag) {
@@ -269,8 +273,8 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         __syncwarp();
     } else if (warp == C::WARP_MMA) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t kQK = idesc_dense(FP8 ? kFmtE4M3 : kFmtBF16,
-                                             FP8 ? kFmtE4M3 : kFmtBF16, 0, 0, 128, 128);
+        constexpr uint32_t kQK = idesc_dense(QK16 ? kFmtBF16 : kFmtE4M3,
+                                             QK16 ? kFmtBF16 : kFmtE4M3, 0, 0, 128, 128);
         constexpr uint32_t kPV16 = idesc_dense(kFmtBF16, kFmtBF16, 0, 1, 128, 128);
         // descriptors of the operand bases; a K step or stage only adds its
         // byte offset / 16 to the start-address field
@@ -290,7 +294,7 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int kk = 0; kk < C::QK_STEPS; ++kk) {
                 const int off = kk * 32;
                 const int ch = off / C::CB, in = off % C::CB;
-                mma_ss_elect<FP8 ? 1 : 0>(
+                mma_ss_elect<QK16 ? 0 : 1>(
                     d, dq0 + static_cast<uint64_t>((ch * (C::BM * C::CB) + in) >> 4),
                     dk + static_cast<uint64_t>((ch * (C::BN * C::CB) + in) >> 4), kQK,
                     kk > 0 ? 1u : 0u);
@@ -379,7 +383,7 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const float dq = args.descale_q ? *args.descale_q : 1.0f;
         const float dk = args.descale_k ? *args.descale_k : 1.0f;
         const float dv = args.descale_v ? *args.descale_v : 1.0f;
-        const float A1 = FP8 ? args.softmax_scale * dq * dk * kLog2e : args.softmax_scale * kLog2e;
+        const float A1 = QK16 ? args.softmax_scale * kLog2e : args.softmax_scale * dq * dk * kLog2e;
         const float a_lean = A1 * (8.0f / 256.0f);
         if constexpr (FP8) {
             if (wg == 0) tmem_st4(t_row + C::COL_SFB, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu,

@@ -71,9 +71,11 @@ Layout4 layout_of(const long long* st, int Hq, int Hkv, int N, int d_qk, int d_v
 
 // TMA needs byte strides that are positive multiples of 16 below 2^40; the
 // output rows are written 16 bytes at a time.
-int check_strides(const Layout4& L, int esz) {
+int check_strides(const Layout4& L, int qk_esz, int v_esz) {
     const Strides* in[3] = {&L.q, &L.k, &L.v};
-    for (const Strides* s : in) {
+    for (int i = 0; i < 3; ++i) {
+        const Strides* s = in[i];
+        const int esz = i < 2 ? qk_esz : v_esz;
         const long long v[3] = {s->b, s->n, s->h};
         for (long long x : v) {
             if (x <= 0) return ZYFA_ERR_SHAPE;
@@ -131,19 +133,19 @@ int launch2(const void* q, const void* k, const void* v, const FwdArgs& a, const
     return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
 }
 
-template <bool FP8, int DQK>
+template <bool FP8, int DQK, bool QK16 = !FP8>
 int launch(const void* q, const void* k, const void* v, const FwdArgs& a, const Layout4& L,
            cudaStream_t stream) {
-    using C = FwdCfg<FP8, DQK>;
+    using C = FwdCfg<FP8, DQK, QK16>;
     CUtensorMap tq, tk, tv;
     const CUtensorMapSwizzle swz =
         C::CB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     const int inner = C::CB / C::ESZ;
-    if (!make_map(&tq, q, !FP8, DQK, a.Hq, a.N, a.B, L.q, inner, swz)) return ZYFA_ERR_CUDA;
-    if (!make_map(&tk, k, !FP8, DQK, a.Hkv, a.N, a.B, L.k, inner, swz)) return ZYFA_ERR_CUDA;
-    if (!make_map(&tv, v, !FP8, C::DV, a.Hkv, a.N, a.B, L.v, 128 / C::ESZ, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!make_map(&tq, q, QK16, DQK, a.Hq, a.N, a.B, L.q, inner, swz)) return ZYFA_ERR_CUDA;
+    if (!make_map(&tk, k, QK16, DQK, a.Hkv, a.N, a.B, L.k, inner, swz)) return ZYFA_ERR_CUDA;
+    if (!make_map(&tv, v, !FP8, C::DV, a.Hkv, a.N, a.B, L.v, 128 / C::VSZ, CU_TENSOR_MAP_SWIZZLE_128B))
         return ZYFA_ERR_CUDA;
-    auto kern = zyfa_fwd_kernel<FP8, DQK>;
+    auto kern = zyfa_fwd_kernel<FP8, DQK, QK16>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
         cudaSuccess)
         return ZYFA_ERR_CUDA;
@@ -185,7 +187,7 @@ extern "C" int zyfa_fwd_strided(const void* q, const void* k, const void* v,
         !aligned(lse, 4))
         return ZYFA_ERR_ALIGN;
     const Layout4 L = layout_of(strides, Hq, Hkv, N, d_qk, d_v);
-    if ((rc = check_strides(L, 1)) != ZYFA_OK) return rc;
+    if ((rc = check_strides(L, 1, 1)) != ZYFA_OK) return rc;
     FwdArgs a{out, lse, descale_q, descale_k, descale_v, B, Hq, Hkv, N, p_mode, block_scale,
               causal, 1.0f / sqrtf(static_cast<float>(d_qk)), L.o.b, L.o.n, L.o.h};
     auto s = static_cast<cudaStream_t>(stream);
@@ -221,7 +223,7 @@ extern "C" int zyfa_fwd_bf16_strided(const void* q, const void* k, const void* v
     if (rc <= 0) return rc;
     if (!aligned(lse, 4)) return ZYFA_ERR_ALIGN;
     const Layout4 L = layout_of(strides, Hq, Hkv, N, d_qk, d_v);
-    if ((rc = check_strides(L, 2)) != ZYFA_OK) return rc;
+    if ((rc = check_strides(L, 2, 2)) != ZYFA_OK) return rc;
     FwdArgs a{out, lse, nullptr, nullptr, nullptr, B, Hq, Hkv, N, 0, 0, causal,
               1.0f / sqrtf(static_cast<float>(d_qk)), L.o.b, L.o.n, L.o.h};
     auto s = static_cast<cudaStream_t>(stream);
@@ -239,6 +241,25 @@ extern "C" int zyfa_fwd_bf16(const void* q, const void* k, const void* v, void* 
                              int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
                              void* stream) {
     return zyfa_fwd_bf16_ex(q, k, v, out, nullptr, B, Hq, Hkv, N, d_qk, d_v, causal, stream);
+}
+
+extern "C" int zyfa_fwd_bf16qk_fp8pv(const void* q, const void* k, const void* v,
+                                     const float* descale_v, void* out, float* lse, int B,
+                                     int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
+                                     int p_mode, int block_scale, const long long* strides,
+                                     void* stream) {
+    int rc = check_common(q, k, v, out, B, Hq, Hkv, N, d_qk, d_v, causal, 2);
+    if (rc <= 0) return rc;
+    if (p_mode != ZYFA_P_EXACT && p_mode != ZYFA_P_LEAN) return ZYFA_ERR_UNSUPPORTED;
+    if (block_scale != 0 && block_scale != 1) return ZYFA_ERR_UNSUPPORTED;
+    if (!aligned(descale_v, 4) || !aligned(lse, 4)) return ZYFA_ERR_ALIGN;
+    const Layout4 L = layout_of(strides, Hq, Hkv, N, d_qk, d_v);
+    if ((rc = check_strides(L, 2, 1)) != ZYFA_OK) return rc;
+    FwdArgs a{out, lse, nullptr, nullptr, descale_v, B, Hq, Hkv, N, p_mode, block_scale,
+              causal, 1.0f / sqrtf(static_cast<float>(d_qk)), L.o.b, L.o.n, L.o.h};
+    auto s = static_cast<cudaStream_t>(stream);
+    return d_qk == 128 ? launch<true, 128, true>(q, k, v, a, L, s)
+                       : launch<true, 192, true>(q, k, v, a, L, s);
 }
 
 extern "C" const char* zyfa_status_string(int status) {

@@ -208,6 +208,25 @@ int zyfa_fwd_bf16_strided(const void* q, const void* k, const void* v, void* out
                           int B, int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
                           const long long* strides, void* stream);
 
+/*
+ * BF16 QK^T with FP8 PV: the variant the paper's conclusion recommends
+ * (V adds the least input error, so keeping QK^T in BF16 and running only PV
+ * in FP8 removes most of the input error).  Q and K are BF16 (no descale),
+ * the scores come from a BF16 MMA, and everything after them is the FP8 path
+ * of zyfa_fwd: running maximum (tau = 0.125), Lean P or exact P codes with
+ * sigma = 6, per-64-key block scaling, the block-scaled e4m3 PV product with
+ * V's descale, division by the rounded row sum.
+ *   q, k        BF16 [B, N, H, d_qk];  v  e4m3 codes [B, N, Hkv, d_v].
+ *   descale_v   one FP32 in device memory, or NULL for 1.0.
+ *   strides     as zyfa_fwd_strided (q and k strides x 2 bytes, v strides
+ *               x 1 byte must be multiples of 16), or NULL for BSHD.
+ * Everything else as zyfa_fwd_ex.
+ */
+int zyfa_fwd_bf16qk_fp8pv(const void* q, const void* k, const void* v, const float* descale_v,
+                          void* out, float* lse, int B, int Hq, int Hkv, int N, int d_qk,
+                          int d_v, int causal, int p_mode, int block_scale,
+                          const long long* strides, void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* zyfa_status_string(int status);
 
