@@ -20,6 +20,10 @@ FlashAttention on AMD CDNA4"):
 * ``max_mode`` 0: the exact row maximum used to emulate the P term,
   Sec. V-E "Error of each stage of one call";
 * ``attn_fp64``: fp64 attention on the quantised inputs, Sec. V-D, fn. 15;
+* ``key_begin`` / ``key_end`` and ``merge``: partial attention over a key
+  range and the merge of partial results by their LSE (Sec. IV-B3: the LSE
+  lets results over different key ranges be merged); the running maximum of
+  a range starts at its first key;
 * ``dtype='mixed'``: BF16 QK^T with the FP8 PV path, the variant the
   conclusion recommends (keep QK^T in BF16, run only PV in FP8); read as the
   e4m3 method (tau = 0.125, sigma = 6, block scaling, rounded denominator)
@@ -79,6 +83,7 @@ class Params(ctypes.Structure):
         ("denom_mode", ctypes.c_int),
         ("sigma", ctypes.c_double), ("beta", ctypes.c_double),
         ("o_max", ctypes.c_int),
+        ("key_begin", ctypes.c_int), ("key_end", ctypes.c_int),
     ]
 
 
@@ -181,7 +186,8 @@ def make_params(*, dtype: str, B: int, Hq: int, Hkv: int, N: int, d_qk: int,
                 p_mode: int = P_LEAN, block_scale: int = 1,
                 max_mode: int = MAX_RUNNING, tau=None, kv_block: int = KV_BLOCK,
                 scale_block: int = SCALE_BLOCK, denom_mode=None, sigma=None,
-                beta: float = BETA, causal: int = 1, o_max: int = O_MAX) -> Params:
+                beta: float = BETA, causal: int = 1, o_max: int = O_MAX,
+                key_begin: int = 0, key_end: int = -1) -> Params:
     """Parameters with the method's defaults for ``dtype``: 'e4m3', 'bf16', or
     'mixed' (BF16 Q and K, e4m3 V: the FP8 probability path of the e4m3
     kernels after a BF16 QK^T; Q and K carry no descale)."""
@@ -206,7 +212,8 @@ def make_params(*, dtype: str, B: int, Hq: int, Hkv: int, N: int, d_qk: int,
                   float(descale[0]), float(descale[1]), float(descale[2]),
                   float(softmax_scale), int(p_mode), int(block_scale),
                   int(max_mode), float(tau), int(kv_block), int(scale_block),
-                  int(denom_mode), float(sigma), float(beta), int(o_max))
+                  int(denom_mode), float(sigma), float(beta), int(o_max),
+                  int(key_begin), int(key_end))
 
 
 def _prep(p: Params, q, k, v, rows):
@@ -264,6 +271,25 @@ def attn_fp64(p: Params, q, k, v, rows=None, nthreads=None):
     if rc:
         raise ValueError(f"oracle zo_attn_fp64 failed with status {rc}")
     return out, lse
+
+
+def merge(outs, lses):
+    """Combine partial attention results over disjoint key ranges (Sec. IV-B3:
+    the LSE is returned so that results over different key ranges can be
+    merged): with L = ln sum_i exp(LSE_i), O = sum_i exp(LSE_i - L) O_i.  Rows
+    that no range reaches get O = 0 and L = -inf.  float64 throughout."""
+    outs = [np.asarray(o, dtype=np.float64) for o in outs]
+    lses = np.stack([np.asarray(l, dtype=np.float64) for l in lses])     # [P, R]
+    top = np.max(lses, axis=0)
+    live = np.isfinite(top)
+    safe = np.where(live, top, 0.0)
+    w = np.exp(lses - safe)                                             # exp(-inf) = 0
+    tot = w.sum(axis=0)
+    L = np.where(live, safe + np.log(np.where(live, tot, 1.0)), -np.inf)
+    out = np.zeros_like(outs[0])
+    for wi, oi in zip(w, outs):
+        out += np.where(live, wi / np.where(live, tot, 1.0), 0.0)[:, None] * oi
+    return out, L
 
 
 def bf16_bits_to_f64(bits) -> np.ndarray:

@@ -173,6 +173,8 @@ typedef struct {
     double sigma;         /* probability shift (6 in FP8, 0 in BF16)          */
     double beta;          /* Lean P bias (0.35)                               */
     int o_max;            /* largest block exponent (UE8M0 range: 127)        */
+    int key_begin;        /* keys [key_begin, key_end) only (split-key       */
+    int key_end;          /* partial attention, Sec. IV-B3); key_end < 0: N   */
 } zo_params;
 
 static double e4m3_table[256];
@@ -228,8 +230,11 @@ typedef struct {
     long long next;       /* shared work counter                              */
 } zo_job;
 
-/* Scores of row r: fills t[j] = c * dq * dk * log2(e) * (q_i . k_j) for the
- * visible keys and returns their count. */
+/* First key of the range. */
+static inline int key0(const zo_params* p) { return p->key_begin > 0 ? p->key_begin : 0; }
+
+/* Scores of row r: fills t[j] = c * dq * dk * log2(e) * (q_i . k_(key0 + j))
+ * for the visible keys of the key range and returns their count. */
 static int row_scores(const zo_params* p, const void* q, const void* k,
                       long long r, double* qv, double* t)
 {
@@ -238,15 +243,19 @@ static int row_scores(const zo_params* p, const void* q, const void* k,
     int h = (int)((r / N) % Hq);
     int i = (int)(r % N);
     int g = h / (Hq / p->Hkv);
-    int nk = p->causal ? i + 1 : N;
+    int kend = p->causal ? i + 1 : N;
+    if (p->key_end >= 0 && p->key_end < kend) kend = p->key_end;
+    int nk = kend - key0(p);
+    if (nk < 0) nk = 0;
     size_t qoff = (((size_t)b * N + i) * Hq + h) * (size_t)p->d_qk;
     for (int d = 0; d < p->d_qk; ++d) qv[d] = load_qk(p, q, qoff + d);
     double cst = p->softmax_scale * p->descale_q * p->descale_k * M_LOG2E;
-    for (int j = 0; j < nk; ++j) {
+    for (int jj = 0; jj < nk; ++jj) {
+        const int j = key0(p) + jj;
         size_t koff = (((size_t)b * N + j) * p->Hkv + g) * (size_t)p->d_qk;
         double s = 0.0;
         for (int d = 0; d < p->d_qk; ++d) s += qv[d] * load_qk(p, k, koff + d);
-        t[j] = cst * s;
+        t[jj] = cst * s;
     }
     return nk;
 }
@@ -254,7 +263,7 @@ static int row_scores(const zo_params* p, const void* q, const void* k,
 static inline void add_value(const zo_params* p, const void* v, long long b,
                              int g, int j, double w, double* acc)
 {
-    size_t voff = (((size_t)b * p->N + j) * p->Hkv + g) * (size_t)p->d_v;
+    size_t voff = (((size_t)b * p->N + key0(p) + j) * p->Hkv + g) * (size_t)p->d_v;
     for (int d = 0; d < p->d_v; ++d) acc[d] += w * load_v(p, v, voff + d);
 }
 
@@ -279,6 +288,11 @@ static void method_row(const zo_params* p, const void* v, long long r,
     for (int d = 0; d < p->d_v; ++d) acc[d] = 0.0;
     double l = 0.0;
     double m_ref = -INFINITY;
+    if (nk == 0) {        /* no visible key in the range: nothing to merge */
+        for (int d = 0; d < p->d_v; ++d) out[d] = 0.0;
+        if (lse_out) *lse_out = -INFINITY;
+        return;
+    }
 
     int seg = p->max_mode == 0 ? nk : p->kv_block;
     if (p->max_mode == 0)
@@ -335,6 +349,11 @@ static void reference_row(const zo_params* p, const void* v, long long r,
     long long b = r / ((long long)Hq * N);
     int h = (int)((r / N) % Hq);
     int g = h / (Hq / p->Hkv);
+    if (nk == 0) {
+        for (int d = 0; d < p->d_v; ++d) out[d] = 0.0;
+        if (lse_out) *lse_out = -INFINITY;
+        return;
+    }
     double m = -INFINITY;
     for (int j = 0; j < nk; ++j) m = nanmax(m, t[j] * M_LN2);
     for (int d = 0; d < p->d_v; ++d) acc[d] = 0.0;

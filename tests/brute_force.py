@@ -100,7 +100,7 @@ def decode(a, dtype):
 
 def forward(q, k, v, *, dtype, descale, p_mode, block_scale, max_mode, tau,
             kv_block, scale_block, denom_mode, sigma, beta, softmax_scale,
-            o_max=127):
+            o_max=127, key_begin=0, key_end=None):
     """Full (B, N, Hq, d_v) output in float64, all rows, causal.  dtype
     'mixed': BF16 Q and K, e4m3 V and e4m3 probabilities."""
     B, N, Hq, dqk = q.shape
@@ -117,8 +117,12 @@ def forward(q, k, v, *, dtype, descale, p_mode, block_scale, max_mode, tau,
             g = h // grp
             T = (Q[b, :, h, :] @ K[b, :, g, :].T) * (softmax_scale * dq * dk / math.log(2.0))
             for i in range(N):
-                t = T[i, :i + 1]
-                nk = i + 1
+                kb = key_begin
+                ke = i + 1 if key_end is None else min(i + 1, key_end)
+                if ke <= kb:
+                    continue                       # nothing visible: output 0
+                t = T[i, kb:ke]
+                nk = ke - kb
                 if max_mode == 0:
                     segs = [(0, nk, float(np.max(t)))]
                 else:
@@ -141,7 +145,7 @@ def forward(q, k, v, *, dtype, descale, p_mode, block_scale, max_mode, tau,
                         o = int(min(max(math.floor(m - hm), 0), o_max)) if block_scale else 0
                         pr, pu = prob(t[j] - m + o, dtype, p_mode, sigma, beta)
                         w = pr * 2.0 ** -o
-                        num += f * w * V[b, j, g, :]
+                        num += f * w * V[b, kb + j, g, :]
                         den += f * (w if denom_mode == 0 else pu * 2.0 ** -o)
                 out[b, i, h, :] = dvs * num / den
     return out

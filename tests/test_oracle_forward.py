@@ -330,3 +330,81 @@ def test_mixed_equals_e4m3_on_shared_values(p_mode):
     _, out8, _, _ = _run(q8, k8, v8, (1.0, 1.0, dvs), "e4m3", p_mode=p_mode)
     _, outm, _, _ = _run(q16, k16, v8, (1.0, 1.0, dvs), "mixed", p_mode=p_mode)
     assert np.array_equal(out8, outm)
+
+
+# ---------------------------------------------------------------------------
+# key ranges and the merge of partial results (Sec. IV-B3)
+# ---------------------------------------------------------------------------
+def _run_range(q, k, v, ds, dtype, kb, ke, **kw):
+    B, N, Hq, dqk = q.shape
+    p = oracle.make_params(dtype=dtype, B=B, Hq=Hq, Hkv=k.shape[2], N=N, d_qk=dqk,
+                           d_v=v.shape[3], descale=ds, key_begin=kb, key_end=ke, **kw)
+    out, outb, lse = oracle.fwd(p, q, k, v)
+    return p, out, lse
+
+
+def test_full_key_range_equals_forward():
+    q, k, v, ds = _tiny(1, 200, 2, 1, 16, 8, seed=41)
+    _, out_full, lse_full = _run_range(q, k, v, ds, "e4m3", 0, 200)
+    p = oracle.make_params(dtype="e4m3", B=1, Hq=2, Hkv=1, N=200, d_qk=16, d_v=8, descale=ds)
+    out, _, lse = oracle.fwd(p, q, k, v)
+    assert np.array_equal(out_full, out) and np.array_equal(lse_full, lse)
+
+
+@pytest.mark.parametrize("p_mode,block_scale", [(0, 1), (1, 1), (1, 0)])
+@pytest.mark.parametrize("kb,ke", [(0, 128), (128, 256), (128, 300), (256, 300)])
+def test_key_range_matches_brute_force(p_mode, block_scale, kb, ke):
+    q, k, v, ds = _tiny(1, 300, 2, 1, 16, 8, seed=42)
+    p, out, _ = _run_range(q, k, v, ds, "e4m3", kb, ke, p_mode=p_mode, block_scale=block_scale,
+                           kv_block=128, scale_block=64)
+    ref = bf.forward(q, k, v, dtype="e4m3", descale=ds, p_mode=p.p_mode,
+                     block_scale=p.block_scale, max_mode=p.max_mode, tau=p.tau,
+                     kv_block=p.kv_block, scale_block=p.scale_block, denom_mode=p.denom_mode,
+                     sigma=p.sigma, beta=p.beta, softmax_scale=p.softmax_scale,
+                     key_begin=kb, key_end=ke)
+    out = out.reshape(1, 2, 300, 8).transpose(0, 2, 1, 3)
+    assert _rel(out, ref) < 1e-12
+    # rows that see no key of the range: zero output
+    if kb > 0:
+        assert not out[:, :kb].any()
+
+
+def test_empty_range_gives_zero_and_minus_inf():
+    q, k, v, ds = _tiny(1, 256, 1, 1, 16, 8, seed=43)
+    _, out, lse = _run_range(q, k, v, ds, "e4m3", 128, 256)
+    out = out.reshape(256, 8)
+    assert not out[:128].any() and np.all(np.isneginf(lse[:128]))
+    assert np.all(np.isfinite(lse[128:]))
+
+
+@pytest.mark.parametrize("dtype", ["e4m3", "bf16"])
+def test_merge_of_unrounded_ranges_is_fp64_attention(dtype):
+    """With unrounded p each range is exact softmax attention over its keys,
+    and the LSE-weighted merge of softmax over disjoint key sets is softmax
+    over their union: the merge must give fp64 attention and its LSE."""
+    q, k, v, ds = _tiny(2, 320, 2, 1, 16, 8, seed=44, dtype=dtype)
+    p = oracle.make_params(dtype=dtype, B=2, Hq=2, Hkv=1, N=320, d_qk=16, d_v=8, descale=ds)
+    ref, ref_lse = oracle.attn_fp64(p, q, k, v)
+    parts = [_run_range(q, k, v, ds, dtype, kb, ke, p_mode=2)[1:]
+             for kb, ke in ((0, 128), (128, 256), (256, 320))]
+    out, lse = oracle.merge([o for o, _ in parts], [l for _, l in parts])
+    assert _rel(out, ref) < 1e-12
+    assert np.max(np.abs(lse - ref_lse)) < 1e-10
+    # and the fp64 reference over ranges merges to the same
+    ref_parts = []
+    for kb, ke in ((0, 128), (128, 256), (256, 320)):
+        pr = oracle.make_params(dtype=dtype, B=2, Hq=2, Hkv=1, N=320, d_qk=16, d_v=8,
+                                descale=ds, key_begin=kb, key_end=ke)
+        ref_parts.append(oracle.attn_fp64(pr, q, k, v))
+    out2, lse2 = oracle.merge([o for o, _ in ref_parts], [l for _, l in ref_parts])
+    assert _rel(out2, ref) < 1e-12 and np.max(np.abs(lse2 - ref_lse)) < 1e-10
+
+
+def test_merge_single_part_is_identity():
+    rng = np.random.default_rng(3)
+    o = rng.standard_normal((10, 4))
+    l = rng.standard_normal(10)
+    l[3] = -np.inf
+    out, L = oracle.merge([o], [l])
+    assert np.allclose(out[np.isfinite(l)], o[np.isfinite(l)], rtol=0, atol=1e-15)
+    assert np.array_equal(L, l) and not out[3].any()
