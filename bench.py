@@ -364,7 +364,60 @@ def extras(args, P, fp8_peak, bf16_peak):
     res["d128_lean_bhsd"] = {"tflops": tf, "ms": ms, "frac_of_peak": tf / fp8_peak}
     del qs, ks, vs, out
     torch.cuda.empty_cache()
+    res.update(split_extras(steps, fp8_peak))
     res.update(quant_extras(steps))
+    return res
+
+
+def split_extras(steps, fp8_peak):
+    """Split-key attention on the d=128 workload (Lean P): keys [0, N/2) and
+    [N/2, N) as two partial calls, then the LSE merge (Sec. IV-B3).  The
+    whole step is quoted in TFLOP/s of the full causal attention; the merge
+    kernel alone in GB/s against HBM, algorithmic bytes per row = n_parts x
+    (2 d_v + 4) read + (2 d_v + 4) written."""
+    import torch
+    import fp8_causal_flashattention_gb300 as Z
+    from tests import parity as P
+    peaks, _ = measured_peaks()
+    wl = S.WORKLOADS["d128"]
+    inp = S.make_inputs(wl)
+    (q, k, v), ds = P.to_device(inp)
+    del inp
+    shape = (wl.B, wl.N, wl.Hq, wl.d_v)
+    outs = [torch.empty(shape, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    lses = [torch.empty((wl.B, wl.Hq, wl.N), dtype=torch.float32, device="cuda")
+            for _ in range(2)]
+    out = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((wl.B, wl.Hq, wl.N), dtype=torch.float32, device="cuda")
+    half = wl.N // 2
+    stream = torch.cuda.current_stream()
+
+    def parts():
+        for i, (a, b) in enumerate(((0, half), (half, wl.N))):
+            Z.attention_partial(q, k, v, ds[0], ds[1], ds[2], key_begin=a, key_end=b,
+                                out=outs[i], lse=lses[i])
+
+    def merge():
+        rc = Z.zyfa_merge(outs, lses, out, lse, wl.B, wl.Hq, wl.N, wl.d_v, stream)
+        if rc != Z.ZYFA_OK:
+            raise Z.ZyfaError(rc, "zyfa_merge")
+
+    def step():
+        parts()
+        merge()
+
+    ms = time_launches(step, steps, 3, stream)
+    ms_merge = time_launches(merge, steps, 3, stream)
+    rows = wl.B * wl.Hq * wl.N
+    nbytes = rows * (2 * (2 * wl.d_v + 4) + (2 * wl.d_v + 4))
+    gbs = nbytes / (ms_merge * 1e-3) / 1e9
+    tf = wl.causal_flops / (ms * 1e-3) / 1e12
+    res = {"d128_lean_split2_merge": {"tflops": tf, "ms": ms, "frac_of_peak": tf / fp8_peak,
+                                      "launches": 3},
+           "merge_d128_2parts": {"ms": ms_merge, "gbs": gbs,
+                                 "frac_of_hbm": gbs / peaks["hbm_gbs"], "bytes": nbytes}}
+    del q, k, v, outs, lses, out, lse
+    torch.cuda.empty_cache()
     return res
 
 

@@ -31,6 +31,7 @@ ZYFA_P_LEAN = 1
 
 EXPORTS = ("zyfa_fwd", "zyfa_fwd_bf16", "zyfa_fwd_ex", "zyfa_fwd_bf16_ex",
            "zyfa_fwd_strided", "zyfa_fwd_bf16_strided", "zyfa_fwd_bf16qk_fp8pv",
+           "zyfa_fwd_partial", "zyfa_fwd_bf16_partial", "zyfa_merge",
            "zyfa_quantize", "zyfa_quantize_noalloc", "zyfa_status_string", "zyfa_last_device_status", "zyfa_selftest_timeout",
            "zyfa_version")
 
@@ -69,6 +70,12 @@ def load():
     lib.zyfa_fwd_bf16qk_fp8pv.restype = ci
     lib.zyfa_fwd_bf16qk_fp8pv.argtypes = [vp] * 6 + [ci] * 9 + [vp, vp]
     lib.zyfa_quantize.restype = ci
+    lib.zyfa_fwd_partial.argtypes = [vp] * 8 + [ci] * 11 + [vp, vp]
+    lib.zyfa_fwd_partial.restype = ci
+    lib.zyfa_fwd_bf16_partial.argtypes = [vp] * 5 + [ci] * 9 + [vp, vp]
+    lib.zyfa_fwd_bf16_partial.restype = ci
+    lib.zyfa_merge.argtypes = [vp, vp, ci, vp, vp] + [ci] * 4 + [vp]
+    lib.zyfa_merge.restype = ci
     lib.zyfa_quantize.argtypes = [vp, vp, ci, ctypes.c_float, vp, vp, vp] + [ci] * 4 + [vp]
     lib.zyfa_quantize_noalloc.restype = ci
     lib.zyfa_quantize_noalloc.argtypes = lib.zyfa_quantize.argtypes
@@ -186,6 +193,40 @@ def zyfa_fwd_bf16qk_fp8pv(q, k, v, descale_v, out, lse, B, Hq, Hkv, N, d_qk, d_v
                                         _stream(stream))
 
 
+def zyfa_fwd_partial(q, k, v, descale_q, descale_k, descale_v, out, lse, B, Hq, Hkv, N, d_qk,
+                     d_v, causal=1, p_mode=ZYFA_P_LEAN, block_scale=1, key_begin=0,
+                     key_end=None, strides=None, stream=None) -> int:
+    """``zyfa_fwd_partial`` of include/zyfa.h (``key_end`` None: N)."""
+    sa = _strides_arg(strides)
+    return load().zyfa_fwd_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(descale_q), _ptr(descale_k),
+                                   _ptr(descale_v), _ptr(out), _ptr(lse), B, Hq, Hkv, N, d_qk,
+                                   d_v, causal, p_mode, block_scale, key_begin,
+                                   N if key_end is None else key_end,
+                                   None if sa is None else sa[0], _stream(stream))
+
+
+def zyfa_fwd_bf16_partial(q, k, v, out, lse, B, Hq, Hkv, N, d_qk, d_v, causal=1, key_begin=0,
+                          key_end=None, strides=None, stream=None) -> int:
+    """``zyfa_fwd_bf16_partial`` of include/zyfa.h (``key_end`` None: N)."""
+    sa = _strides_arg(strides)
+    return load().zyfa_fwd_bf16_partial(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq,
+                                        Hkv, N, d_qk, d_v, causal, key_begin,
+                                        N if key_end is None else key_end,
+                                        None if sa is None else sa[0], _stream(stream))
+
+
+def zyfa_merge(outs, lses, out, lse, B, Hq, N, d_v, stream=None) -> int:
+    """``zyfa_merge`` of include/zyfa.h: ``outs`` / ``lses`` are sequences of
+    tensors or device addresses (marshalled into host pointer arrays)."""
+    n = len(outs)
+    if len(lses) != n:
+        raise ValueError("outs and lses must have the same length")
+    po = (ctypes.c_void_p * max(n, 1))(*[_ptr(o) for o in outs])
+    pl = (ctypes.c_void_p * max(n, 1))(*[_ptr(x) for x in lses])
+    return load().zyfa_merge(ctypes.cast(po, ctypes.c_void_p), ctypes.cast(pl, ctypes.c_void_p),
+                             n, _ptr(out), _ptr(lse), B, Hq, N, d_v, _stream(stream))
+
+
 def zyfa_status_string(status: int) -> str:
     return load().zyfa_status_string(int(status)).decode()
 
@@ -299,4 +340,51 @@ def attention_bf16qk_fp8pv(q, k, v, descale_v=None, *, p_mode=ZYFA_P_LEAN, block
                                p_mode, block_scale, _layout(q, k, v, out), stream)
     if rc != ZYFA_OK:
         raise ZyfaError(rc, "zyfa_fwd_bf16qk_fp8pv")
+    return (out, lse) if return_lse else out
+
+
+def attention_partial(q, k, v, descale_q=None, descale_k=None, descale_v=None, *, key_begin=0,
+                      key_end=None, p_mode=ZYFA_P_LEAN, block_scale=1, causal=1, out=None,
+                      lse=None, stream=None):
+    """Attention over the keys [key_begin, key_end) (multiples of 128).  FP8
+    when q is float8_e4m3fn / uint8 (descales as attention_fp8), BF16 when q
+    is bfloat16.  Returns (out, lse); rows that see no key of the range get
+    0 and -inf."""
+    import torch
+    B, N, Hq, Hkv, d_qk, d_v = _shape(q, k, v)
+    if out is None:
+        out = torch.empty((B, N, Hq, d_v), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    st = _layout(q, k, v, out)
+    if q.dtype == torch.bfloat16:
+        rc = zyfa_fwd_bf16_partial(q, k, v, out, lse, B, Hq, Hkv, N, d_qk, d_v, causal,
+                                   key_begin, key_end, st, stream)
+    else:
+        rc = zyfa_fwd_partial(q, k, v, descale_q, descale_k, descale_v, out, lse, B, Hq, Hkv, N,
+                              d_qk, d_v, causal, p_mode, block_scale, key_begin, key_end, st,
+                              stream)
+    if rc != ZYFA_OK:
+        raise ZyfaError(rc, "zyfa_fwd_partial")
+    return out, lse
+
+
+def merge(outs, lses, *, out=None, return_lse=True, stream=None):
+    """Merge partial results (BF16 [B, N, Hq, d_v] contiguous, FP32 LSE
+    [B, Hq, N]) over disjoint key ranges.  Returns out (and the merged LSE)."""
+    import torch
+    if not outs:
+        raise ValueError("nothing to merge")
+    B, N, Hq, d_v = outs[0].shape
+    for o, l in zip(outs, lses):
+        if tuple(o.shape) != (B, N, Hq, d_v) or not o.is_contiguous() or \
+                tuple(l.shape) != (B, Hq, N) or not l.is_contiguous():
+            raise ValueError("parts must be contiguous [B, N, Hq, d_v] with LSE [B, Hq, N]")
+    if out is None:
+        out = torch.empty((B, N, Hq, d_v), dtype=torch.bfloat16, device=outs[0].device)
+    lse = (torch.empty((B, Hq, N), dtype=torch.float32, device=outs[0].device)
+           if return_lse else None)
+    rc = zyfa_merge(outs, lses, out, lse, B, Hq, N, d_v, stream)
+    if rc != ZYFA_OK:
+        raise ZyfaError(rc, "zyfa_merge")
     return (out, lse) if return_lse else out

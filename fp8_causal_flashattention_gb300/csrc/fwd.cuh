@@ -55,6 +55,11 @@ struct FwdArgs {
     int causal;                    // 1: key j visible to query i iff j <= i; 0: all keys
     float softmax_scale;           // c
     long long o_sb, o_sn, o_sh;    // element strides of out per batch, position, head
+    // Key range [128 kb0, 128 kb1) in 128-key blocks: a call over part of the
+    // keys, whose outputs are merged by their LSE (Sec. IV-B3).  The default
+    // is every key.  Only the one-tile kernel reads these.
+    int kb0 = 0;
+    int kb1 = 1 << 30;
 };
 
 // FP8: e4m3 V and probabilities (the PV path); QK16: Q and K in BF16 (the
@@ -190,7 +195,28 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int b = bg / args.Hkv;
     const int g = bg % args.Hkv;
     const int h = g * grp + rem % grp;
-    const int nblk = args.causal ? qt + 1 : T;
+    const int lim = args.causal ? qt + 1 : T;
+    const int kend = lim < args.kb1 ? lim : args.kb1;
+    const int nblk = kend > args.kb0 ? kend - args.kb0 : 0;   // blocks kb0 .. kend-1
+
+    if (nblk == 0) {
+        // No key of the range is visible to this tile: O = 0 and LSE = -inf,
+        // the identity of the merge.  Nothing has been set up yet.
+        const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+        for (int e = threadIdx.x; e < C::BM * (C::DV / 8); e += C::THREADS) {
+            const int r = e / (C::DV / 8);
+            const long long orow = b * args.o_sb +
+                                   (static_cast<long long>(qt) * C::BM + r) * args.o_sn + h * args.o_sh;
+            reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + orow)[e % (C::DV / 8)] =
+                zero;
+        }
+        if (args.lse) {
+            const size_t base = (static_cast<size_t>(b) * args.Hq + h) * args.N +
+                                static_cast<size_t>(qt) * C::BM;
+            for (int r = threadIdx.x; r < C::BM; r += C::THREADS) args.lse[base + r] = -INFINITY;
+        }
+        return;
+    }
 
     if (threadIdx.x == 0) {
         mbar_init(BAR(B_QF), 1);
@@ -252,12 +278,12 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             #pragma unroll
             for (int c = 0; c < C::NCH; ++c)
                 tma_load_4d_elect(sbase + C::OFF_K + st * C::K_BYTES + c * (C::BN * C::CB), &tm_k,
-                                  BAR(B_KF + st), c * C::CB / C::ESZ, g, i * C::BN, b);
+                                  BAR(B_KF + st), c * C::CB / C::ESZ, g, (args.kb0 + i) * C::BN, b);
             mbar_expect_tx_elect(BAR(B_VF + st), C::V_BYTES);
             #pragma unroll
             for (int c = 0; c < C::VCH; ++c)
                 tma_load_4d_elect(sbase + C::OFF_V + st * C::V_BYTES + c * (C::BN * 128), &tm_v,
-                                  BAR(B_VF + st), c * 128 / C::VSZ, g, i * C::BN, b);
+                                  BAR(B_VF + st), c * 128 / C::VSZ, g, (args.kb0 + i) * C::BN, b);
             ++issued;
         }
         if (*abort_flag) {
@@ -411,7 +437,7 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // S_i is in registers: QK_{i+2} may overwrite the buffer
             tc_fence_before();
             mbar_arrive(BAR(B_SX + wg));
-            if (args.causal && i == nblk - 1) {             // diagonal block: key > query
+            if (args.causal && args.kb0 + i == qt) {        // diagonal block: key > query
                 #pragma unroll
                 for (int j = 0; j < 128; ++j)
                     if (j > row) s[j] = -INFINITY;

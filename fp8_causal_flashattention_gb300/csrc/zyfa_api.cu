@@ -243,6 +243,57 @@ extern "C" int zyfa_fwd_bf16(const void* q, const void* k, const void* v, void* 
     return zyfa_fwd_bf16_ex(q, k, v, out, nullptr, B, Hq, Hkv, N, d_qk, d_v, causal, stream);
 }
 
+// Key range of the partial calls: multiples of 128 keys within [0, N].
+static int check_range(int N, int key_begin, int key_end) {
+    if (key_begin < 0 || key_end < key_begin || key_end > N) return ZYFA_ERR_SHAPE;
+    if (key_begin % 128 != 0 || key_end % 128 != 0) return ZYFA_ERR_SHAPE;
+    return ZYFA_OK;
+}
+
+extern "C" int zyfa_fwd_partial(const void* q, const void* k, const void* v,
+                                const float* descale_q, const float* descale_k,
+                                const float* descale_v, void* out, float* lse, int B, int Hq,
+                                int Hkv, int N, int d_qk, int d_v, int causal, int p_mode,
+                                int block_scale, int key_begin, int key_end,
+                                const long long* strides, void* stream) {
+    int rc = check_common(q, k, v, out, B, Hq, Hkv, N, d_qk, d_v, causal, 1);
+    if (rc < 0) return rc;
+    if (check_range(N, key_begin, key_end) != ZYFA_OK) return ZYFA_ERR_SHAPE;
+    if (rc == 0) return ZYFA_OK;                      // empty problem
+    if (!lse) return ZYFA_ERR_NULL;                   // the merge weighs the parts by it
+    if (p_mode != ZYFA_P_EXACT && p_mode != ZYFA_P_LEAN) return ZYFA_ERR_UNSUPPORTED;
+    if (block_scale != 0 && block_scale != 1) return ZYFA_ERR_UNSUPPORTED;
+    if (!aligned(descale_q, 4) || !aligned(descale_k, 4) || !aligned(descale_v, 4) ||
+        !aligned(lse, 4))
+        return ZYFA_ERR_ALIGN;
+    const Layout4 L = layout_of(strides, Hq, Hkv, N, d_qk, d_v);
+    if ((rc = check_strides(L, 1, 1)) != ZYFA_OK) return rc;
+    FwdArgs a{out, lse, descale_q, descale_k, descale_v, B, Hq, Hkv, N, p_mode, block_scale,
+              causal, 1.0f / sqrtf(static_cast<float>(d_qk)), L.o.b, L.o.n, L.o.h,
+              key_begin / 128, key_end / 128};
+    auto s = static_cast<cudaStream_t>(stream);
+    return d_qk == 128 ? launch<true, 128>(q, k, v, a, L, s) : launch<true, 192>(q, k, v, a, L, s);
+}
+
+extern "C" int zyfa_fwd_bf16_partial(const void* q, const void* k, const void* v, void* out,
+                                     float* lse, int B, int Hq, int Hkv, int N, int d_qk,
+                                     int d_v, int causal, int key_begin, int key_end,
+                                     const long long* strides, void* stream) {
+    int rc = check_common(q, k, v, out, B, Hq, Hkv, N, d_qk, d_v, causal, 2);
+    if (rc < 0) return rc;
+    if (check_range(N, key_begin, key_end) != ZYFA_OK) return ZYFA_ERR_SHAPE;
+    if (rc == 0) return ZYFA_OK;                      // empty problem
+    if (!lse) return ZYFA_ERR_NULL;                   // the merge weighs the parts by it
+    if (!aligned(lse, 4)) return ZYFA_ERR_ALIGN;
+    const Layout4 L = layout_of(strides, Hq, Hkv, N, d_qk, d_v);
+    if ((rc = check_strides(L, 2, 2)) != ZYFA_OK) return rc;
+    FwdArgs a{out, lse, nullptr, nullptr, nullptr, B, Hq, Hkv, N, 0, 0, causal,
+              1.0f / sqrtf(static_cast<float>(d_qk)), L.o.b, L.o.n, L.o.h, key_begin / 128,
+              key_end / 128};
+    auto s = static_cast<cudaStream_t>(stream);
+    return d_qk == 128 ? launch<false, 128>(q, k, v, a, L, s) : launch<false, 192>(q, k, v, a, L, s);
+}
+
 extern "C" int zyfa_fwd_bf16qk_fp8pv(const void* q, const void* k, const void* v,
                                      const float* descale_v, void* out, float* lse, int B,
                                      int Hq, int Hkv, int N, int d_qk, int d_v, int causal,

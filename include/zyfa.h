@@ -227,6 +227,54 @@ int zyfa_fwd_bf16qk_fp8pv(const void* q, const void* k, const void* v, const flo
                           int d_v, int causal, int p_mode, int block_scale,
                           const long long* strides, void* stream);
 
+/*
+ * Attention over the keys [key_begin, key_end) only: the split-key form of
+ * the forward.  The paper returns the LSE so that results over different key
+ * ranges can be merged (Sec. IV-B3); this call gives one such result and
+ * zyfa_merge combines them (to spread one long sequence over more SMs, or to
+ * combine results computed over separate parts of K and V).
+ * The method runs on the range's keys alone: query i sees key j iff
+ * key_begin <= j < key_end and (causal) j <= i; the running maximum, the
+ * lazy rescale and the block scales start at key_begin.  Rows that see no
+ * key of the range get out = 0 and lse = -inf (the merge's identity).
+ *   key_begin, key_end   multiples of 128, 0 <= key_begin <= key_end <= N
+ *                        (ZYFA_ERR_SHAPE otherwise);
+ *   lse                  required (ZYFA_ERR_NULL when NULL), FP32 [B, Hq, N].
+ * Everything else as zyfa_fwd_strided (strides NULL for BSHD).  Always one
+ * query tile per CTA.  Merging disjoint ranges that cover [0, N) gives
+ * attention over all keys up to the BF16 rounding of each part and the
+ * per-range choices of maximum and block scale.
+ */
+int zyfa_fwd_partial(const void* q, const void* k, const void* v,
+                     const float* descale_q, const float* descale_k, const float* descale_v,
+                     void* out, float* lse, int B, int Hq, int Hkv, int N, int d_qk, int d_v,
+                     int causal, int p_mode, int block_scale, int key_begin, int key_end,
+                     const long long* strides, void* stream);
+
+/* zyfa_fwd_partial for BF16 inputs (the zyfa_fwd_bf16 method over a range). */
+int zyfa_fwd_bf16_partial(const void* q, const void* k, const void* v, void* out, float* lse,
+                          int B, int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
+                          int key_begin, int key_end, const long long* strides, void* stream);
+
+/*
+ * Merge of partial results over disjoint key ranges by their LSE
+ * (Sec. IV-B3).  Per row, in FP32: M = max_i LSE_i, L = M + ln sum_i
+ * exp(LSE_i - M), out = BF16_RNE(sum_i exp(LSE_i - L) O_i); rows whose LSEs
+ * are all -inf get out = 0 and L = -inf.
+ *   outs      host array of n_parts device pointers, BF16 [B, N, Hq, d_v]
+ *             contiguous, 16-byte aligned;
+ *   lses      host array of n_parts device pointers, FP32 [B, Hq, N];
+ *   n_parts   1 .. 16 (ZYFA_ERR_SHAPE below, ZYFA_ERR_UNSUPPORTED above);
+ *   out       BF16 [B, N, Hq, d_v], caller-owned; may be one of outs;
+ *   lse       FP32 [B, Hq, N] for L, or NULL; must not be one of lses
+ *             (ZYFA_ERR_UNSUPPORTED);
+ *   d_v       a multiple of 8 up to 4096.
+ * The arrays outs and lses are read during the call only.  Asynchronous on
+ * `stream`; allocates nothing.
+ */
+int zyfa_merge(const void* const* outs, const float* const* lses, int n_parts, void* out,
+               float* lse, int B, int Hq, int N, int d_v, void* stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char* zyfa_status_string(int status);
 

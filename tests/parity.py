@@ -65,7 +65,10 @@ def gather_rows(out, wl: S.Workload, rows) -> np.ndarray:
     return sel.float().cpu().numpy().astype(np.float64)
 
 
-def oracle_params(wl: S.Workload, inp: S.Inputs, mode: str, max_mode=None, causal: int = 1):
+def oracle_params(wl: S.Workload, inp: S.Inputs, mode: str, max_mode=None, causal: int = 1,
+                  **extra):
+    """Oracle parameters of a GPU mode; ``extra`` (e.g. key_begin / key_end)
+    passes through to oracle.make_params."""
     import oracle
     if max_mode is None:
         max_mode = oracle.MAX_RUNNING
@@ -76,6 +79,7 @@ def oracle_params(wl: S.Workload, inp: S.Inputs, mode: str, max_mode=None, causa
         kw.update(descale=inp.descale,
                   p_mode=oracle.P_LEAN if mode.startswith("lean") else oracle.P_EXACT,
                   block_scale=0 if mode.endswith("nobs") else 1)
+    kw.update(extra)
     return oracle.make_params(**kw)
 
 

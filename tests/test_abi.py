@@ -141,3 +141,59 @@ def test_strided_argument_errors(lib, which, bad, want):
     rc = Z.zyfa_fwd_strided(FAKE, FAKE, FAKE, None, None, None, FAKE, None, 1, 2, 1, 256, 128, 128,
                             1, 1, 1, flat, 0)
     assert rc == want
+
+
+@pytest.mark.parametrize("fp8", [True, False])
+@pytest.mark.parametrize("kb,ke,lse,want", [
+    (64, 256, FAKE, Z.ZYFA_ERR_SHAPE),       # not a multiple of 128
+    (0, 200, FAKE, Z.ZYFA_ERR_SHAPE),
+    (256, 128, FAKE, Z.ZYFA_ERR_SHAPE),      # end before begin
+    (-128, 128, FAKE, Z.ZYFA_ERR_SHAPE),
+    (0, 512, FAKE, Z.ZYFA_ERR_SHAPE),        # past N
+    (0, 256, 0, Z.ZYFA_ERR_NULL),            # the LSE is required
+])
+def test_partial_argument_errors(lib, fp8, kb, ke, lse, want):
+    N = 256
+    if fp8:
+        rc = Z.zyfa_fwd_partial(FAKE, FAKE, FAKE, None, None, None, FAKE, lse, 1, 2, 1, N, 128,
+                                128, key_begin=kb, key_end=ke, stream=0)
+    else:
+        rc = Z.zyfa_fwd_bf16_partial(FAKE, FAKE, FAKE, FAKE, lse, 1, 2, 1, N, 128, 128,
+                                     key_begin=kb, key_end=ke, stream=0)
+    assert rc == want
+
+
+def test_partial_empty_problem_is_ok(lib):
+    assert Z.zyfa_fwd_partial(0, 0, 0, None, None, None, 0, None, 0, 2, 1, 256, 128, 128,
+                              key_begin=0, key_end=256, stream=0) == Z.ZYFA_OK
+    assert Z.zyfa_fwd_bf16_partial(0, 0, 0, 0, None, 1, 2, 1, 0, 128, 128, key_begin=0,
+                                   key_end=0, stream=0) == Z.ZYFA_OK
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(outs=[], lses=[]), Z.ZYFA_ERR_SHAPE),
+    (dict(outs=[FAKE] * 17, lses=[FAKE] * 17), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(outs=[FAKE, 0], lses=[FAKE, FAKE]), Z.ZYFA_ERR_NULL),
+    (dict(outs=[FAKE, FAKE], lses=[FAKE, 0]), Z.ZYFA_ERR_NULL),
+    (dict(out=0), Z.ZYFA_ERR_NULL),
+    (dict(outs=[FAKE, FAKE + 8], lses=[FAKE, FAKE]), Z.ZYFA_ERR_ALIGN),
+    (dict(lses=[FAKE, FAKE + 2]), Z.ZYFA_ERR_ALIGN),
+    (dict(out=FAKE + 4), Z.ZYFA_ERR_ALIGN),
+    (dict(lse=FAKE + 1), Z.ZYFA_ERR_ALIGN),
+    (dict(lse=FAKE + 4096), Z.ZYFA_ERR_UNSUPPORTED),     # the merged LSE in place
+    (dict(d_v=12), Z.ZYFA_ERR_SHAPE),
+    (dict(d_v=0), Z.ZYFA_ERR_SHAPE),
+    (dict(Hq=0), Z.ZYFA_ERR_SHAPE),
+    (dict(B=-1), Z.ZYFA_ERR_SHAPE),
+])
+def test_merge_argument_errors(lib, kw, want):
+    a = dict(outs=[FAKE, FAKE], lses=[FAKE, FAKE + 4096], out=FAKE, lse=None, B=1, Hq=2, N=256,
+             d_v=128)
+    a.update(kw)
+    assert Z.zyfa_merge(a["outs"], a["lses"], a["out"], a["lse"], a["B"], a["Hq"], a["N"],
+                        a["d_v"], stream=0) == want
+
+
+def test_merge_empty_problem_is_ok(lib):
+    assert Z.zyfa_merge([FAKE], [FAKE], FAKE, None, 0, 2, 256, 128, stream=0) == Z.ZYFA_OK
+    assert Z.zyfa_merge([FAKE], [FAKE], FAKE, None, 1, 2, 0, 128, stream=0) == Z.ZYFA_OK
