@@ -266,9 +266,9 @@ int zyfa_fwd_bf16_partial(const void* q, const void* k, const void* v, void* out
  *   lses      host array of n_parts device pointers, FP32 [B, Hq, N];
  *   n_parts   1 .. 16 (ZYFA_ERR_SHAPE below, ZYFA_ERR_UNSUPPORTED above);
  *   out       BF16 [B, N, Hq, d_v], caller-owned; may be one of outs;
- *   lse       FP32 [B, Hq, N] for L, or NULL; must not be one of lses
- *             (ZYFA_ERR_UNSUPPORTED);
- *   d_v       a multiple of 8 up to 4096.
+ *   lse       FP32 [B, Hq, N] for L, or NULL; may be one of lses;
+ *   d_v       a power of two from 8 to 4096; B x Hq x N below 2^31
+ *             (ZYFA_ERR_SHAPE otherwise).
  * The arrays outs and lses are read during the call only.  Asynchronous on
  * `stream`; allocates nothing.
  */

@@ -180,8 +180,9 @@ def test_partial_empty_problem_is_ok(lib):
     (dict(lses=[FAKE, FAKE + 2]), Z.ZYFA_ERR_ALIGN),
     (dict(out=FAKE + 4), Z.ZYFA_ERR_ALIGN),
     (dict(lse=FAKE + 1), Z.ZYFA_ERR_ALIGN),
-    (dict(lse=FAKE + 4096), Z.ZYFA_ERR_UNSUPPORTED),     # the merged LSE in place
     (dict(d_v=12), Z.ZYFA_ERR_SHAPE),
+    (dict(d_v=24), Z.ZYFA_ERR_SHAPE),                    # not a power of two
+    (dict(N=1 << 30, Hq=2), Z.ZYFA_ERR_SHAPE),           # B Hq N >= 2^31
     (dict(d_v=0), Z.ZYFA_ERR_SHAPE),
     (dict(Hq=0), Z.ZYFA_ERR_SHAPE),
     (dict(B=-1), Z.ZYFA_ERR_SHAPE),

@@ -190,10 +190,11 @@ def test_merge_empty_parts_and_in_place(lib):
     o0, l0 = _partial(lib, dev, mode, 0, 256)
     o2, l2 = _partial(lib, dev, mode, 128, 128)
     ref, ref_lse = _merge_ref([(o0, l0), (o1, l1), (o2, l2)], wl, rows)
-    copy, _ = lib.merge([o0, o1, o2], [l0, l1, l2])
-    lib.merge([o0, o1, o2], [l0, l1, l2], out=o0, return_lse=False)
+    copy, copy_lse = lib.merge([o0, o1, o2], [l0, l1, l2])
+    rc = lib.zyfa_merge([o0, o1, o2], [l0, l1, l2], o0, l0, wl.B, wl.Hq, wl.N, wl.d_v)
+    assert rc == lib.ZYFA_OK
     torch.cuda.synchronize()
-    assert bool((copy == o0).all())
+    assert bool((copy == o0).all()) and bool((copy_lse == l0).all())
     got, _ = _decoded(o0, l0, wl, rows)
     assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) * (1 + 1e-4) + 1e-6)
 
@@ -224,3 +225,22 @@ def test_full_size_split_sampled_rows(lib):
     print("full size split: rel_l2", rel, "lse max", err.max())
     assert rel <= STRICT_REL_L2
     assert err.max() <= 2e-2 and np.sqrt(np.mean(err ** 2)) <= 5e-4
+
+
+@pytest.mark.parametrize("mode", ["lean", "bf16"])
+def test_merge_many_parts(lib, mode):
+    """One part per 128-key block (5 parts, the templated kernels), and the
+    same with empty parts added (12 parts, the general kernel): both against
+    the float64 merge, and equal to each other (an empty part weighs 0)."""
+    import torch
+    wl, inp, dev = _inputs(("gqa", 2, 4, 2, 640, 128), mode, seed=16)
+    rows = np.arange(wl.B * wl.Hq * wl.N)
+    parts = [_partial(lib, dev, mode, a, a + 128) for a in range(0, wl.N, 128)]
+    empty = [_partial(lib, dev, mode, 256, 256) for _ in range(7)]
+    out5, lse5 = lib.merge([o for o, _ in parts], [l for _, l in parts])
+    mixed = parts[:2] + empty + parts[2:]
+    out12, lse12 = lib.merge([o for o, _ in mixed], [l for _, l in mixed])
+    got, got_lse = _decoded(out5, lse5, wl, rows)
+    ref, ref_lse = _merge_ref(parts, wl, rows)
+    _check_merge(got, got_lse, ref, ref_lse)
+    assert bool((out5 == out12).all()) and bool((lse5 == lse12).all())
