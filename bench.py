@@ -502,6 +502,45 @@ def run_sweep(args):
             torch.cuda.empty_cache()
 
 
+def run_accuracy(args):
+    """Fig. 15's measurement on this GPU: the output error of one call on
+    each synthetic input at S = 8K, as relative RMS against fp64 attention on
+    the same quantised inputs (sampled rows, 64 per head), for Lean P, exact
+    P and BF16, next to the oracle's ablation in the style of the compared
+    FP8 kernel (exact p rounded relative to the row maximum, no block
+    scaling, unrounded row sum).  One JSON line per input and head size."""
+    import torch
+    import oracle
+    import fp8_causal_flashattention_gb300 as Z
+    from tests import accuracy as A
+    from tests import parity as P
+    Z.load()
+    torch.cuda.set_device(0)
+    for d in (128, 192):
+        for kind in list(S.FIG15_KINDS) + ["far_blocks"]:
+            wl = S.Workload(kind, 1, 8, 8, 8192, d, 128, kind=kind)
+            rows = S.sample_rows(wl, per_head=64)
+            line = {"input": kind, "d_qk": d, "d_v": 128, "N": wl.N, "Hq": wl.Hq,
+                    "rows": int(len(rows)), "metric": "rel RMS vs fp64 on the same inputs"}
+            inp = S.make_inputs(wl, fp8=True, bf16=True)
+            ref8, _ = oracle.attn_fp64(P.oracle_params(wl, inp, "lean"), inp.q8, inp.k8, inp.v8,
+                                       rows)
+            ref16, _ = oracle.attn_fp64(P.oracle_params(wl, inp, "bf16"), inp.q16, inp.k16,
+                                        inp.v16, rows)
+            for mode in ("lean", "exact", "bf16"):
+                out = P.gpu_run(inp, mode)
+                got = P.gather_rows(out, wl, rows)
+                line[mode] = A.rel_rms(got, ref16 if mode == "bf16" else ref8)
+                del out
+            _, ob, _ = oracle.fwd(A.ablation_params(wl, inp), inp.q8, inp.k8, inp.v8, rows)
+            line["ablation"] = A.rel_rms(oracle.bf16_bits_to_f64(ob), ref8)
+            line["lean_over_ablation"] = line["lean"] / line["ablation"]
+            line["exact_over_ablation"] = line["exact"] / line["ablation"]
+            print(json.dumps(line), flush=True)
+            del inp
+            torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -515,9 +554,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--sweep", action="store_true",
                     help="time every workload and mode (one JSON line each)")
+    ap.add_argument("--accuracy", action="store_true",
+                    help="error of one call on Fig. 15's synthetic inputs (one JSON line each)")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)
+        return
+    if args.accuracy:
+        run_accuracy(args)
         return
     wl = S.WORKLOADS[args.workload]
     if args.impl == "reference":

@@ -123,7 +123,7 @@ class Workload:
     N: int
     d_qk: int
     d_v: int
-    kind: str = "gaussian"          # "gaussian", "activation", "sink" or "kbias"
+    kind: str = "gaussian"          # "gaussian", "activation", "sink", "kbias" or FIG15_KINDS
     note: str = ""
 
     @property
@@ -184,6 +184,14 @@ def fp32_qkv(wl: Workload, seed: int = SEED):
         q, k, meta = _sink(wl, q, k)
     elif wl.kind == "kbias":
         k, meta = _kbias(wl, k, seed)
+    elif wl.kind in FIG15_KINDS:
+        q, k, v, meta = _fig15(wl, q, k, v, seed)
+    elif wl.kind == "far_blocks":
+        q, k, meta = _sink(wl, q, k)
+        v = v + np.float32(FAR_BLOCKS_V_MEAN)
+        meta["v_mean"] = FAR_BLOCKS_V_MEAN
+    elif wl.kind != "gaussian":
+        raise ValueError(f"unknown input kind {wl.kind!r}")
     return q, k, v, meta
 
 
@@ -295,6 +303,13 @@ def _sink(wl: Workload, q, k, gap: float = SINK_GAP):
     return q, k, {"sink_gap": gap}
 
 
+# Blocks far below the row maximum that still carry mass, and values with a
+# common direction (real value vectors have non-zero means): the pattern of
+# Fig. 5, where probabilities lost to rounding bias the output instead of
+# averaging out.
+FAR_BLOCKS_V_MEAN = 1.0
+
+
 # --------------------------------------------------------------------------
 # keys with a shared offset
 # --------------------------------------------------------------------------
@@ -308,3 +323,83 @@ def _kbias(wl: Workload, k, seed: int):
     sequence, which K smoothing removes."""
     bias = normal((wl.B, 1, wl.Hkv, wl.d_qk), seed, KBIAS_STREAM) * np.float32(KBIAS_SCALE)
     return k + bias, {"kbias_scale": KBIAS_SCALE}
+
+
+# --------------------------------------------------------------------------
+# the synthetic accuracy inputs of Fig. 15 ("ZYFA: Speed and Accuracy of FP8
+# FlashAttention on AMD CDNA4", Sec. VI, Fig. 15), from their descriptions
+# --------------------------------------------------------------------------
+FIG15_KINDS = ("f15_gaussian", "logit_sd1", "logit_sd4", "logit_sd16", "stepped_max", "sink4",
+               "rising", "alternating", "sink_flat", "full_range")
+F15_SIGMA = 0.1              # Gaussian: q, k, v ~ N(0, 0.1^2)
+F15_STEP_NATS = 1.0          # Stepped Max: logit step per 64-key block (not printed)
+F15_RAMP_NATS = 16.0         # Rising / Alternating: total rise over the keys (not printed)
+F15_SINK_NATS = 12.0         # Sink + Flat Tail: first key above the rest
+F15_FLAT_SD = 0.1            # Sink + Flat Tail: logit SD of the "nearly uniform" rest
+F15_SINK4_GAIN = 8.0         # 4-Key Sink: the first four keys scaled by 8
+F15_RANGE = (-6.0, 8.0)      # Full Range: log2 of the magnitude, uniform
+F15_CH_GAIN = 4.0            # value of the query channel that carries a key-side offset
+STREAM_F15_U = 4             # streams 4, 5, 6: the uniforms of q, k, v (Full Range)
+
+
+def _logit_offset(wl: Workload, q, k, ch: int, per_key, rows=None):
+    """Add per_key[j] nats to the logit q_i . k_j / sqrt(d_qk) of every query
+    row i (or of the rows selected by the boolean ``rows`` mask) through one
+    channel: q[..., ch] = F15_CH_GAIN there (0 elsewhere) and k[:, j, :, ch] =
+    per_key[j] sqrt(d_qk) / F15_CH_GAIN."""
+    q[..., ch] = np.float32(F15_CH_GAIN)
+    if rows is not None:
+        q[:, ~rows, :, ch] = 0.0
+    k[:, :, :, ch] = (np.asarray(per_key, dtype=np.float64) * np.sqrt(wl.d_qk)
+                      / F15_CH_GAIN).astype(np.float32)[None, :, None]
+
+
+def _uniform(shape, seed: int, stream: int) -> np.ndarray:
+    """Uniform (0, 1) values as the normal CDF of the stream's N(0, 1) draws."""
+    from scipy.special import ndtr
+    return ndtr(normal(shape, seed, stream).astype(np.float64))
+
+
+def _fig15(wl: Workload, q, k, v, seed: int):
+    """Fig. 15's inputs from their descriptions, on standard normal q, k, v
+    (where the figure leaves a size open the constant above is this
+    module's reading):
+      f15_gaussian   q, k, v ~ N(0, 0.1^2) (the timing runs' draw);
+      logit_sd{1,4,16}  q and k scaled by 1, 2, 4: logits with SD 1, 4, 16 nats;
+      stepped_max    each successive 64-key block F15_STEP_NATS higher;
+      sink4          the first four keys scaled by 8;
+      rising         a linear ramp along the keys, F15_RAMP_NATS over N keys;
+      alternating    the same ramp on every other query row (even rows);
+      sink_flat      q, k scaled to a logit SD of F15_FLAT_SD, key 0 raised
+                     F15_SINK_NATS above them;
+      full_range     every element of q, k, v: a random sign times 2^u, u
+                     uniform in [-6, 8]."""
+    kind = wl.kind
+    N = wl.N
+    j = np.arange(N, dtype=np.float64)
+    meta = {"fig15": kind}
+    if kind == "f15_gaussian":
+        q, k, v = (x * np.float32(F15_SIGMA) for x in (q, k, v))
+    elif kind.startswith("logit_sd"):
+        g = np.float32(np.sqrt(float(kind[len("logit_sd"):])))
+        q, k = q * g, k * g
+    elif kind == "stepped_max":
+        _logit_offset(wl, q, k, 0, F15_STEP_NATS * (j // 64))
+    elif kind == "sink4":
+        k[:, :4] *= np.float32(F15_SINK4_GAIN)
+    elif kind in ("rising", "alternating"):
+        rows = (np.arange(N) % 2 == 0) if kind == "alternating" else None
+        _logit_offset(wl, q, k, 0, F15_RAMP_NATS * j / N, rows)
+    elif kind == "sink_flat":
+        g = np.float32(np.sqrt(F15_FLAT_SD))
+        q, k = q * g, k * g
+        _logit_offset(wl, q, k, 0, np.where(j == 0, F15_SINK_NATS, 0.0))
+    elif kind == "full_range":
+        lo, hi = F15_RANGE
+        out = []
+        for t, x in enumerate((q, k, v)):
+            u = _uniform(x.shape, seed, STREAM_F15_U + t)
+            mag = np.exp2(lo + (hi - lo) * u)
+            out.append((np.sign(x) * mag).astype(np.float32))
+        q, k, v = out
+    return q, k, v, meta

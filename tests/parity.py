@@ -117,6 +117,9 @@ def errors(gpu_rows: np.ndarray, inp: S.Inputs, mode: str, rows, extra: bool = T
         res["rel_l2_exactmax"] = float(np.linalg.norm(gpu_rows - refe) / np.linalg.norm(refe))
         res["rel_l2_fp64"] = float(np.linalg.norm(gpu_rows - ref64) / np.linalg.norm(ref64))
         res["oracle_rel_l2_fp64"] = float(np.linalg.norm(ref - ref64) / np.linalg.norm(ref64))
+        # the oracle's output rounded to BF16 as the kernels' (the like-for-like distance)
+        res["oracle_bf16_rel_l2_fp64"] = float(np.linalg.norm(ref_b - ref64) /
+                                               np.linalg.norm(ref64))
     return res
 
 
