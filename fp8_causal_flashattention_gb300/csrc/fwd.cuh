@@ -149,6 +149,14 @@ __device__ __forceinline__ uint32_t lean_word(float s, float a, float b) {
     return __float_as_uint(fmaf(z, 256.0f, 12582912.0f));
 }
 
+// (a, b) *= f on the bit patterns of two FP32 values, one packed multiply.
+__device__ __forceinline__ void mul2s(uint32_t& a, uint32_t& b, float f) {
+    asm("{\n\t.reg .b64 Z, K;\n\t"
+        "mov.b64 Z, {%0, %1};\n\tmov.b64 K, {%2, %2};\n\t"
+        "mul.rn.f32x2 Z, Z, K;\n\tmov.b64 {%0, %1}, Z;\n\t}"
+        : "+r"(a), "+r"(b) : "f"(f));
+}
+
 // Named barrier over the softmax warps that also ANDs a predicate across
 // them, so that every thread takes the same branch afterwards.
 __device__ __forceinline__ bool bar_and(int id, int nthreads, bool pred) {
@@ -566,21 +574,19 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 ok2 = __all_sync(0xffffffffu, ok2);
                 if (ok2) {
                     tc_fence_after();
+                    uint32_t lr = 0;
+                    if constexpr (FP8) tmem_ld1(t_row + C::COL_L, lr);     // waited with chunk 0
                     #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t r[32];
                         tmem_ld32(t_row + C::COL_O + c * 32, r);
                         tmem_wait_ld();
                         #pragma unroll
-                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * f);
+                        for (int j = 0; j < 32; j += 2) mul2s(r[j], r[j + 1], f);
                         tmem_st<32>(t_row + C::COL_O + c * 32, r);
                     }
-                    if constexpr (FP8) {
-                        uint32_t lr;
-                        tmem_ld1(t_row + C::COL_L, lr);
-                        tmem_wait_ld();
+                    if constexpr (FP8)
                         tmem_st1(t_row + C::COL_L, __float_as_uint(__uint_as_float(lr) * f));
-                    }
                 }
             }
             tmem_wait_st();

@@ -304,7 +304,24 @@ zyfa_fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             if (did) {
                 t_prog = globaltimer();
-            } else if (*abort_flag) {
+                continue;
+            }
+            // Nothing ready: sleep in the wait for the next P (the PV side is
+            // the latency-critical one; a load found ready late still lands
+            // blocks before its QK), instead of spinning on the issue slots
+            // that this SM sub-partition's softmax warps need.
+            if (pj < nbt) {
+                const int st = pj % C::NST;
+                const bool pf = __all_sync(0xffffffffu, mbar_test(BAR(B_PF + t), pj & 1));
+                (void)__all_sync(0xffffffffu,
+                                 pf ? mbar_try_for(BAR(B_VF + st), (pj / C::NST) & 1, kIdleWaitNs)
+                                    : mbar_try_for(BAR(B_PF + t), pj & 1, kIdleWaitNs));
+            } else {
+                const int st = li % C::NST;
+                (void)__all_sync(0xffffffffu,
+                                 mbar_try_for(BAR(B_KE + st), ((li / C::NST) - 1) & 1, kIdleWaitNs));
+            }
+            if (*abort_flag) {
                 ok = false;
             } else if (globaltimer() - t_prog > kWaitBudgetNs) {
                 *abort_flag = 1;
@@ -459,18 +476,17 @@ zyfa_fwd2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 tc_fence_after();
             }
             if (j > 0 && __any_sync(0xffffffffu, f != 1.0f)) {
+                uint32_t lr;
+                tmem_ld1(t_row + C::col_l(t), lr);
                 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     uint32_t r[32];
                     tmem_ld32(t_row + C::col_o(t) + c * 32, r);
                     tmem_wait_ld();
                     #pragma unroll
-                    for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * f);
-                    tmem_st<32>(t_row + C::col_o(t) + c * 32, r);
+                    for (int k = 0; k < 32; k += 2) mul2s(r[k], r[k + 1], f);
+                    tmem_st32(t_row + C::col_o(t) + c * 32, r);
                 }
-                uint32_t lr;
-                tmem_ld1(t_row + C::col_l(t), lr);
-                tmem_wait_ld();
                 tmem_st1(t_row + C::col_l(t), __float_as_uint(__uint_as_float(lr) * f));
             }
             tmem_wait_st();

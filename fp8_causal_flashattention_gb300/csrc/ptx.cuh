@@ -10,6 +10,7 @@
 namespace zyfa {
 
 constexpr unsigned long long kWaitBudgetNs = 1500ull * 1000ull * 1000ull;   // 1.5 s
+constexpr uint32_t kIdleWaitNs = 500;   // longest sleep of a polling issuer with nothing to do
 
 // Device status word read back by zyfa_last_device_status().
 //   0 = ok; otherwise (site << 8) | 1 for a wait that ran out.
@@ -51,6 +52,17 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
                  "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
                  "selp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// As mbar_try, but the thread may stay suspended in the wait for up to about
+// `ns` nanoseconds (it resumes as soon as the phase completes).
+__device__ __forceinline__ bool mbar_try_for(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity), "r"(ns) : "memory");
     return ok != 0;
 }
 
