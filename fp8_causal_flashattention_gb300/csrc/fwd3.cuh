@@ -1,0 +1,546 @@
+// fwd3.cuh -- FP8 attention forward with two query tiles per CTA and two
+// softmax warpgroups per tile (sm_103a).
+//
+// Same method as fwd.cuh and fwd2.cuh ("ZYFA: Speed and Accuracy of FP8
+// FlashAttention on AMD CDNA4": running maximum with lazy rescaling, Sec.
+// II-B and IV-A; Lean P and exact P, Sec. IV-B1; per-64-key block scaling,
+// Sec. IV-B2; division by the sum of the rounded probabilities, Sec. IV-B3),
+// with the loads, MMAs, barriers and TMEM map of fwd2.cuh.  What differs is
+// the softmax: each tile has one warpgroup per 64-key score half.  Half h of
+// block j is read by warpgroup h, which releases the score buffer at once
+// (so the tile's next QK half starts), and the two warpgroups exchange their
+// half maxima through two TMEM columns; both then apply the lazy rule to the
+// same numbers (so both hold the same running maximum), each computes the
+// codes of its own 64 keys and writes them into its half of P_j.  The half-1
+// warpgroup also writes the scale factors, waits for PV(j-1), rescales O and
+// L, and publishes P_j together with the half-0 warpgroup (p_full counts
+// both).  Each warpgroup writes 64 of the 128 output columns.
+//
+// Warps 0-15 are softmax (warpgroup w: tile w >> 1, half w & 1); warps 16 /
+// 17 issue QK for tiles A / B, 18 / 19 PV (18 also issues the TMA loads).
+// 640 threads with 96 registers each (one CTA per SM): a softmax thread holds
+// 64 scores instead of fwd2.cuh's 128.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+#include <type_traits>
+
+#include "fwd2.cuh"
+
+namespace zyfa {
+
+template <int DQK>
+struct Fwd3Cfg {
+    static constexpr int NSM = 512;                 // four softmax warpgroups
+    static constexpr int WARP_QK = 16;              // + t: QK issuer of tile t
+    static constexpr int WARP_PV = 18;              // + t: PV issuer of tile t (18: + TMA)
+    static constexpr int THREADS = NSM + 128;
+    static constexpr int BM = 128;                  // rows per query tile
+    static constexpr int BN = 128;                  // keys per block (running-max step)
+    static constexpr int HN = 64;                   // keys per score half
+    static constexpr int DV = 128;
+    static constexpr int CB = DQK == 192 ? 64 : 128;   // bytes per Q/K chunk row
+    static constexpr int NCH = DQK / CB;
+    static constexpr uint32_t SWZ = CB == 128 ? kSwizzle128B : kSwizzle64B;
+    static constexpr int Q_BYTES = BM * DQK;        // one tile
+    static constexpr int K_BYTES = BN * DQK;
+    static constexpr int V_BYTES = BN * DV;
+    static constexpr int P_BYTES = BM * BN;         // one tile, K-major, 128-byte swizzle
+    static constexpr int NST = DQK == 128 ? 4 : 2;
+    static constexpr int QK_STEPS = DQK / 32;       // 32 bytes of K per MMA
+    static constexpr int PV_STEPS = BN / 32;
+    static constexpr int ONES_BYTES = 2048;         // 16 x 128 e4m3 ones
+    static constexpr int OFF_Q = 0;                 // tiles A, B
+    static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
+    static constexpr int OFF_V = OFF_K + NST * K_BYTES;
+    static constexpr int OFF_P = OFF_V + NST * V_BYTES;
+    static constexpr int OFF_ONES = OFF_P + 4 * P_BYTES;   // [tile][slot]
+    static constexpr int OFF_BAR = OFF_ONES + ONES_BYTES;
+    // q_full, k_full[NST], v_full[NST], kv_empty[NST], s_full[2], s_free[2],
+    // p_full[2], o_done[2], fin[2], mma_done[4]; then the TMEM slot and the
+    // abort flag
+    static constexpr int NBAR = 1 + 3 * NST + 12 + 4 + 2;
+    static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16;
+    static constexpr int SMEM_ALLOC = SMEM_BYTES;
+    static __host__ __device__ constexpr uint32_t col_s(int t) { return 64u * t; }
+    static __host__ __device__ constexpr uint32_t col_o(int t) { return 128u + 128u * t; }
+    static __host__ __device__ constexpr uint32_t col_l(int t) { return 384u + 16u * t; }
+    static __host__ __device__ constexpr uint32_t col_sfa(int t, int slot) { return 416u + 16u * t + 4u * slot; }
+    static __host__ __device__ constexpr uint32_t col_sfb(int t) { return 424u + 16u * t; }
+    // half maxima exchanged between a tile's two warpgroups, by block parity
+    static __host__ __device__ constexpr uint32_t col_x(int t, int hf, int par) { return 448u + 4u * t + 2u * hf + par; }
+    static constexpr uint32_t TMEM_COLS = 512;
+};
+
+template <int DQK>
+__global__ void __launch_bounds__(Fwd3Cfg<DQK>::THREADS, 1)
+zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
+    using C = Fwd3Cfg<DQK>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const uint32_t sbase = smem_u32(smem);
+    if (sbase & 1023u) {
+        if (threadIdx.x == 0) atomicCAS(&g_device_status, 0, (9 << 8) | 2);
+        return;
+    }
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+    const uint32_t bar0 = smem_u32(bars);
+    auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+    const int B_QF = 0, B_KF = 1, B_VF = 1 + C::NST, B_KE = 1 + 2 * C::NST;
+    // s_full: [tile][half], one phase per block, so each half's warpgroup
+    // waits on a barrier of its own (a shared one would run up to three
+    // phases ahead of the slower warpgroup, beyond what a parity wait tells)
+    const int B_SF = 1 + 3 * C::NST, B_SX = B_SF + 4, B_PF = B_SX + 2, B_OD = B_PF + 2;
+    const int B_FIN = B_OD + 2, B_MD = B_FIN + 2;   // B_MD: [4], one per issuer warp
+    const int B_X = B_MD + 4;                        // [2]: a tile's half maxima exchanged
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // CTA order: KV-group major (one K/V head stays in L2 while its query
+    // tiles run), longest pair first, the group's query heads side by side
+    const int T = args.N / C::BM;
+    const int P = (T + 1) / 2;                      // tile pairs per head
+    const int grp = args.Hq / args.Hkv;
+    const int per_group = P * grp;
+    const int bg = static_cast<int>(blockIdx.x) / per_group;
+    const int rem = static_cast<int>(blockIdx.x) % per_group;
+    const int pair = P - 1 - rem / grp;
+    const int b = bg / args.Hkv;
+    const int g = bg % args.Hkv;
+    const int h = g * grp + rem % grp;
+    const int qt0 = 2 * pair;                       // tile A; tile B = qt0 + 1
+    const bool has_b = qt0 + 1 < T;
+    // key blocks of each tile
+    const int nb0 = args.causal ? qt0 + 1 : T;
+    const int nb1 = has_b ? (args.causal ? qt0 + 2 : T) : 0;
+    const int nblk = nb0 > nb1 ? nb0 : nb1;
+
+    if (threadIdx.x == 0) {
+        mbar_init(BAR(B_QF), 1);
+        for (int s = 0; s < C::NST; ++s) {
+            mbar_init(BAR(B_KF + s), 1);
+            mbar_init(BAR(B_VF + s), 1);
+            mbar_init(BAR(B_KE + s), 2);          // one commit per PV issuer
+        }
+        for (int t = 0; t < 4; ++t) mbar_init(BAR(B_SF + t), 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(BAR(B_SX + t), 128);
+            mbar_init(BAR(B_PF + t), 256);           // both warpgroups of the tile
+            mbar_init(BAR(B_OD + t), 1);
+            mbar_init(BAR(B_FIN + t), 1);
+        }
+        for (int k = 0; k < 4; ++k) mbar_init(BAR(B_MD + k), 1);
+        mbar_init(BAR(B_X), 256);
+        mbar_init(BAR(B_X + 1), 256);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == C::WARP_QK) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (warp == C::WARP_PV) {    // B operand of the row-sum MMA: e4m3 ones (0x38)
+        uint32_t* ones = reinterpret_cast<uint32_t*>(smem + C::OFF_ONES);
+        for (int i = lane; i < C::ONES_BYTES / 4; i += 32) ones[i] = 0x38383838u;
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto wait_warp = [&](int bar, uint32_t parity, int site) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(BAR(bar), parity, abort_flag, site));
+    };
+
+    if (warp == C::WARP_QK || warp == C::WARP_QK + 1) {
+        // ------------------------------------------------------------ QK issuers
+        // Per tile: QK(j, 0) needs K_j and, for j > 0, half 1 of block j-1
+        // read (s_free); QK(j, 1) needs half 0 of block j read.  The softmax
+        // releases two halves per block, so s_free completes phases 2j (half
+        // 0) and 2j + 1 (half 1); each waited phase is the next one (its
+        // successor needs a QK this warp has not issued yet).
+        const int t = warp - C::WARP_QK;
+        const int nbt = t ? nb1 : nb0;
+        constexpr uint32_t kQK = idesc_dense(kFmtE4M3, kFmtE4M3, 0, 0, 128, C::HN);
+        const uint64_t dq = smem_desc(sbase + C::OFF_Q + t * C::Q_BYTES, 16, 8 * C::CB, C::SWZ);
+        const uint64_t dk0 = smem_desc(sbase + C::OFF_K, 16, 8 * C::CB, C::SWZ);
+        auto issue_qk = [&](int i, int hf) {
+            const int st = i % C::NST;
+            const uint64_t dk = dk0 + static_cast<uint64_t>((st * C::K_BYTES + hf * C::HN * C::CB) >> 4);
+            #pragma unroll
+            for (int kk = 0; kk < C::QK_STEPS; ++kk) {
+                const int off = kk * 32;
+                const int ch = off / C::CB, in = off % C::CB;
+                mma_ss_elect<1>(tmem + C::col_s(t),
+                                dq + static_cast<uint64_t>((ch * (C::BM * C::CB) + in) >> 4),
+                                dk + static_cast<uint64_t>((ch * (C::BN * C::CB) + in) >> 4), kQK,
+                                kk > 0 ? 1u : 0u);
+            }
+            tc_commit_elect(BAR(B_SF + 2 * t + hf));
+        };
+        bool ok = nbt > 0 && wait_warp(B_QF, 0, 22);
+        for (int j = 0; ok && j < nbt; ++j) {
+            if (j > 0 && !(ok = wait_warp(B_SX + t, 1, 31))) break;       // half 1 of j-1 read
+            if (!(ok = wait_warp(B_KF + j % C::NST, (j / C::NST) & 1, 27))) break;
+            tc_fence_after();
+            issue_qk(j, 0);
+            if (!(ok = wait_warp(B_SX + t, 0, 28))) break;                 // half 0 of j read
+            tc_fence_after();
+            issue_qk(j, 1);
+        }
+        tc_commit_elect(BAR(B_MD + t));
+        unsigned long long t0 = globaltimer();
+        while (!mbar_try(BAR(B_MD + t), 0) && globaltimer() - t0 < kWaitBudgetNs) {}
+        __syncwarp();
+    } else if (warp == C::WARP_PV || warp == C::WARP_PV + 1) {
+        // ------------------------------------------------------------ PV issuers
+        // PV(t, j) needs P_j (p_full) and V_j.  The softmax publishes P_j only
+        // after PV(t, j-1) has completed (o_done), so p_full is never more than
+        // one phase ahead.  o_done(t) completes one phase per PV(t, j).  A K/V
+        // stage is released by one commit from each PV issuer; the only user
+        // of a block (the last causal block, or a CTA with one tile) commits
+        // twice.  Issuer A also loads Q and the K/V ring with TMA: it polls
+        // both kinds of work, so neither waits for the other.
+        const int t = warp - C::WARP_PV;
+        const int nbt = t ? nb1 : nb0;
+        const uint64_t dv0 = smem_desc(sbase + C::OFF_V, 1024, 1024, kSwizzle128B);
+        const uint64_t d10 = smem_desc(sbase + C::OFF_ONES, 16, 1024, kSwizzle128B);
+        auto issue_pv = [&](int i) {
+            const int st = i % C::NST;
+            const uint64_t dp = smem_desc(sbase + C::OFF_P + (2 * t + (i & 1)) * C::P_BYTES, 16, 1024,
+                                          kSwizzle128B);
+            const uint64_t dv = dv0 + static_cast<uint64_t>((st * C::V_BYTES) >> 4);
+            const uint32_t sfa = tmem + C::col_sfa(t, i & 1);
+            const uint32_t sfb = tmem + C::col_sfb(t);
+            #pragma unroll
+            for (int kk = 0; kk < C::PV_STEPS; ++kk) {
+                // 32 keys per MMA: A = P_t (K-major, 32 bytes per K step)
+                const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                mma_ss_mx8_elect(tmem + C::col_o(t), dp + ((kk * 32) >> 4),
+                                 dv + ((kk * 32 * 128) >> 4),
+                                 idesc_mx(kFmtE4M3, kFmtE4M3, 0, 1, 128, 128, kk, kk), sfa, sfb,
+                                 acc);
+                mma_ss_mx8_elect(tmem + C::col_l(t), dp + ((kk * 32) >> 4), d10 + ((kk * 32) >> 4),
+                                 idesc_mx(kFmtE4M3, kFmtE4M3, 0, 0, 128, 16, kk, kk), sfa, sfb,
+                                 acc);
+            }
+            tc_commit_elect(BAR(B_OD + t));
+            if (i == nbt - 1) tc_commit_elect(BAR(B_FIN + t));
+            tc_commit_elect(BAR(B_KE + st));
+            if (!(i < nb0 && i < nb1)) tc_commit_elect(BAR(B_KE + st));
+        };
+        auto load_kv = [&](int i) {
+            const int st = i % C::NST;
+            mbar_expect_tx_elect(BAR(B_KF + st), C::K_BYTES);
+            #pragma unroll
+            for (int c = 0; c < C::NCH; ++c)
+                tma_load_4d_elect(sbase + C::OFF_K + st * C::K_BYTES + c * (C::BN * C::CB), &tm_k,
+                                  BAR(B_KF + st), c * C::CB, g, i * C::BN, b);
+            mbar_expect_tx_elect(BAR(B_VF + st), C::V_BYTES);
+            tma_load_4d_elect(sbase + C::OFF_V + st * C::V_BYTES, &tm_v, BAR(B_VF + st), 0, g,
+                              i * C::BN, b);
+        };
+        int li = 0;                                  // next K/V block to load (issuer A)
+        if (t == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_expect_tx_elect(BAR(B_QF), (has_b ? 2 : 1) * C::Q_BYTES);
+            for (int u = 0; u < (has_b ? 2 : 1); ++u) {
+                #pragma unroll
+                for (int c = 0; c < C::NCH; ++c)
+                    tma_load_4d_elect(sbase + C::OFF_Q + u * C::Q_BYTES + c * (C::BM * C::CB), &tm_q,
+                                      BAR(B_QF), c * C::CB, h, (qt0 + u) * C::BM, b);
+            }
+            for (; li < nblk && li < C::NST; ++li) load_kv(li);
+        }
+        int pj = 0;
+        bool ok = true;
+        if (t == 1) {
+            // no loads to interleave: block on the barriers
+            for (; ok && pj < nbt; ++pj) {
+                if (!(ok = wait_warp(B_PF + 1, pj & 1, 29))) break;
+                if (!(ok = wait_warp(B_VF + pj % C::NST, (pj / C::NST) & 1, 30))) break;
+                tc_fence_after();
+                issue_pv(pj);
+            }
+        }
+        unsigned long long t_prog = globaltimer();
+        while (ok && (pj < nbt || (t == 0 && li < nblk))) {
+            bool did = false;
+            if (t == 0 && li < nblk) {
+                const int st = li % C::NST;
+                if (__all_sync(0xffffffffu, mbar_test(BAR(B_KE + st), ((li / C::NST) - 1) & 1))) {
+                    load_kv(li);
+                    ++li;
+                    did = true;
+                }
+            }
+            if (pj < nbt) {
+                const int st = pj % C::NST;
+                const bool rdy = mbar_test(BAR(B_PF + t), pj & 1) &&
+                                 mbar_test(BAR(B_VF + st), (pj / C::NST) & 1);
+                if (__all_sync(0xffffffffu, rdy)) {
+                    tc_fence_after();
+                    issue_pv(pj);
+                    ++pj;
+                    did = true;
+                }
+            }
+            if (did) {
+                t_prog = globaltimer();
+                continue;
+            }
+            // Nothing ready: sleep in the wait for the next P (the PV side is
+            // the latency-critical one; a load found ready late still lands
+            // blocks before its QK), instead of spinning on the issue slots
+            // that this SM sub-partition's softmax warps need.
+            if (pj < nbt) {
+                const int st = pj % C::NST;
+                const bool pf = __all_sync(0xffffffffu, mbar_test(BAR(B_PF + t), pj & 1));
+                (void)__all_sync(0xffffffffu,
+                                 pf ? mbar_try_for(BAR(B_VF + st), (pj / C::NST) & 1, kIdleWaitNs)
+                                    : mbar_try_for(BAR(B_PF + t), pj & 1, kIdleWaitNs));
+            } else {
+                const int st = li % C::NST;
+                (void)__all_sync(0xffffffffu,
+                                 mbar_try_for(BAR(B_KE + st), ((li / C::NST) - 1) & 1, kIdleWaitNs));
+            }
+            if (*abort_flag) {
+                ok = false;
+            } else if (globaltimer() - t_prog > kWaitBudgetNs) {
+                *abort_flag = 1;
+                atomicCAS(&g_device_status, 0, ((23 + t) << 8) | 1);
+                ok = false;
+            }
+        }
+        tc_commit_elect(BAR(B_MD + 2 + t));
+        unsigned long long t0 = globaltimer();
+        while (!mbar_try(BAR(B_MD + 2 + t), 0) && globaltimer() - t0 < kWaitBudgetNs) {}
+        if (t == 0 && *abort_flag) {
+            // let the loads still in flight land before the CTA exits
+            for (int i = li - C::NST < 0 ? 0 : li - C::NST; i < li; ++i) {
+                const int st = i % C::NST;
+                const uint32_t ph = (i / C::NST) & 1;
+                unsigned long long t1 = globaltimer();
+                while (!mbar_try(BAR(B_KF + st), ph) && globaltimer() - t1 < kWaitBudgetNs) {}
+                while (!mbar_try(BAR(B_VF + st), ph) && globaltimer() - t1 < kWaitBudgetNs) {}
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int wg = warp >> 2;
+        const int t = wg >> 1;                              // tile of this warpgroup
+        const int hf = wg & 1;                              // its 64-key half of each block
+        const int qt = qt0 + t;
+        const int nbt = t ? nb1 : nb0;
+        const int row = threadIdx.x & 127;                  // query row = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t t_row = tmem + lane_off;
+        const uint32_t t_s = t_row + C::col_s(t);
+        const float dq = args.descale_q ? *args.descale_q : 1.0f;
+        const float dk = args.descale_k ? *args.descale_k : 1.0f;
+        const float dv = args.descale_v ? *args.descale_v : 1.0f;
+        const float A1 = args.softmax_scale * dq * dk * kLog2e;
+        const float a_lean = A1 * (8.0f / 256.0f);
+        if (hf == 1 && nbt > 0)
+            tmem_st4(t_row + C::col_sfb(t), 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+        float m_run = -INFINITY;                              // running max (base 2)
+        bool ok = true;
+
+        // e4m3 codes of 16 scores relative to maximum m with block exponent o
+        auto codes16 = [&](const float* q, float m, int o) -> uint4 {
+            uint32_t pw[4];
+            if (args.p_mode == 1) {
+                const float bb = (8.0f * (kSigma + 7.0f + (float)o - m) - kBeta) * (1.0f / 256.0f);
+                #pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    // saturating FMA per score, then the rounding FMA on pairs
+                    uint32_t q0, q1, q2, q3;
+                    lean_word2(fma_sat(q[4 * w + 0], a_lean, bb), fma_sat(q[4 * w + 1], a_lean, bb),
+                               q0, q1);
+                    lean_word2(fma_sat(q[4 * w + 2], a_lean, bb), fma_sat(q[4 * w + 3], a_lean, bb),
+                               q2, q3);
+                    pw[w] = __byte_perm(__byte_perm(q0, q1, 0x0040), __byte_perm(q2, q3, 0x0040),
+                                        0x5410);
+                }
+            } else {
+                const float ee = kSigma + (float)o - m;
+                #pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const float p0 = ex2(fmaf(q[4 * w + 0], A1, ee));
+                    const float p1 = ex2(fmaf(q[4 * w + 1], A1, ee));
+                    const float p2 = ex2(fmaf(q[4 * w + 2], A1, ee));
+                    const float p3 = ex2(fmaf(q[4 * w + 3], A1, ee));
+                    pw[w] = cvt_e4m3x2(p0, p1) | (cvt_e4m3x2(p2, p3) << 16);
+                }
+            }
+            return make_uint4(pw[0], pw[1], pw[2], pw[3]);
+        };
+        // whole binades between the 64-key block maximum and the row maximum
+        auto bexp = [&](float m, float hmax) -> int {
+            if (!args.block_scale) return 0;
+            const float gap = floorf(m - hmax * A1);
+            return gap > 0.0f ? (gap < (float)kOMax ? (int)gap : kOMax) : 0;
+        };
+        for (int j = 0; ok && j < nbt; ++j) {
+            // this warpgroup's score half of block j: read, release, maximum
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(B_SF + 2 * t + hf), j & 1, abort_flag,
+                                                         24 + hf))))
+                break;
+            tc_fence_after();
+            float s[64];
+            {
+                uint32_t r[64];
+                tmem_ld32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                tmem_wait_ld();
+                #pragma unroll
+                for (int k = 0; k < 64; ++k) s[k] = __uint_as_float(r[k]);
+            }
+            tc_fence_before();
+            mbar_arrive(BAR(B_SX + t));
+            if (args.causal && j == qt) {                     // diagonal block: key > query
+                #pragma unroll
+                for (int k = 0; k < 64; ++k)
+                    if (64 * hf + k > row) s[k] = -INFINITY;
+            }
+            float hm;
+            {
+                float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
+                #pragma unroll
+                for (int k = 4; k + 8 <= 64; k += 8) {
+                    a0 = max3(a0, s[k + 0], s[k + 4]);
+                    a1 = max3(a1, s[k + 1], s[k + 5]);
+                    a2 = max3(a2, s[k + 2], s[k + 6]);
+                    a3 = max3(a3, s[k + 3], s[k + 7]);
+                }
+                a0 = fmaxf(a0, s[60]);
+                a1 = fmaxf(a1, s[61]);
+                a2 = fmaxf(a2, s[62]);
+                a3 = fmaxf(a3, s[63]);
+                hm = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+            }
+            // exchange the half maxima through TMEM (the column of block
+            // parity j & 1 is rewritten two blocks later, after the other
+            // warpgroup has passed the next exchange)
+            tmem_st1(t_row + C::col_x(t, hf, j & 1), __float_as_uint(hm));
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(BAR(B_X + t));
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(B_X + t), j & 1, abort_flag, 34))))
+                break;
+            tc_fence_after();
+            uint32_t ho;
+            tmem_ld1(t_row + C::col_x(t, 1 - hf, j & 1), ho);
+            tmem_wait_ld();
+            const float hs0 = hf ? __uint_as_float(ho) : hm;
+            const float hs1 = hf ? hm : __uint_as_float(ho);
+            // lazy rule per row (Sec. IV-A), computed identically by both
+            // warpgroups: adopt the block maximum only when it exceeds the
+            // running one by more than tau
+            const float mb = fmaxf(hs0, hs1) * A1;
+            const bool upd = (j == 0) || (mb - m_run > kTauFp8);
+            const float m_i = upd ? mb : m_run;
+            const float f = (j > 0 && upd) ? ex2(m_run - m_i) : 1.0f;
+            m_run = m_i;
+            const int o0 = bexp(m_i, hs0), o1 = bexp(m_i, hs1);
+            // the codes of this half into P_j's slot j & 1, free since PV(j-2)
+            // completed: the half-1 warpgroup waited for it in block j-1,
+            // before its part of this block's exchange.  Row of P: 16-byte
+            // chunk c (keys 16c..16c+15) at chunk position c ^ (row & 7) of
+            // the row's 128 bytes (128-byte swizzle).
+            uint8_t* prow = smem + C::OFF_P + (2 * t + (j & 1)) * C::P_BYTES + row * 128;
+            #pragma unroll
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<uint4*>(prow + (((4 * hf + c) ^ (row & 7)) << 4)) =
+                    codes16(s + 16 * c, m_i, hf ? o1 : o0);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (hf == 0) {
+                mbar_arrive(BAR(B_PF + t));
+                continue;
+            }
+            // UE8M0 scale 2^-o per 32 keys, repeated over the slot's 4 columns
+            const uint32_t sf0 = static_cast<uint32_t>(127 - o0);
+            const uint32_t sf1 = static_cast<uint32_t>(127 - o1);
+            const uint32_t sfw = sf0 | (sf0 << 8) | (sf1 << 16) | (sf1 << 24);
+            tmem_st4(t_row + C::col_sfa(t, j & 1), sfw, sfw, sfw, sfw);
+            // PV(j-1) must be complete before O / L are rescaled and before
+            // P_j is published (which keeps p_full one phase ahead at most)
+            if (j > 0) {
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(B_OD + t), (j - 1) & 1, abort_flag, 32))))
+                    break;
+                tc_fence_after();
+            }
+            if (j > 0 && __any_sync(0xffffffffu, f != 1.0f)) {
+                uint32_t lr;
+                tmem_ld1(t_row + C::col_l(t), lr);
+                #pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(t_row + C::col_o(t) + c * 32, r);
+                    tmem_wait_ld();
+                    #pragma unroll
+                    for (int k = 0; k < 32; k += 2) mul2s(r[k], r[k + 1], f);
+                    tmem_st32(t_row + C::col_o(t) + c * 32, r);
+                }
+                tmem_st1(t_row + C::col_l(t), __float_as_uint(__uint_as_float(lr) * f));
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(BAR(B_PF + t));
+        }
+        // ------------------------------------------------------------ epilogue
+        // each warpgroup writes 64 of the 128 output columns
+        if (nbt > 0) {
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(BAR(B_FIN + t), 0, abort_flag, 26));
+            if (ok) {
+                tc_fence_after();
+                uint32_t lr;
+                tmem_ld1(t_row + C::col_l(t), lr);
+                tmem_wait_ld();
+                const float l = __uint_as_float(lr);
+                const float inv = dv / l;
+                // LSE of the rounded weights: l is relative to the final
+                // running max and carries the 2^sigma shift (Sec. IV-B3)
+                if (args.lse && hf == 1) {
+                    const size_t lse_idx = (static_cast<size_t>(b) * args.Hq + h) * args.N +
+                                           static_cast<size_t>(qt) * C::BM + row;
+                    args.lse[lse_idx] = logf(l) + (m_run - kSigma) * 0.6931471805599453f;
+                }
+                const long long orow = b * args.o_sb + (static_cast<long long>(qt) * C::BM + row) * args.o_sn +
+                                       h * args.o_sh;
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + orow + 64 * hf);
+                #pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(t_row + C::col_o(t) + 64 * hf + c * 32, r);
+                    tmem_wait_ld();
+                    #pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint4 v4;
+                        v4.x = cvt_bf16x2(__uint_as_float(r[8 * k + 0]) * inv, __uint_as_float(r[8 * k + 1]) * inv);
+                        v4.y = cvt_bf16x2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv);
+                        v4.z = cvt_bf16x2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv);
+                        v4.w = cvt_bf16x2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv);
+                        dst[c * 4 + k] = v4;
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+    }
+    __syncthreads();
+    if (warp == C::WARP_QK) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace zyfa

@@ -10,6 +10,7 @@
 #include "../../include/zyfa.h"
 #include "fwd.cuh"
 #include "fwd2.cuh"
+#include "fwd3.cuh"
 
 namespace zyfa {
 namespace {
@@ -133,6 +134,28 @@ int launch2(const void* q, const void* k, const void* v, const FwdArgs& a, const
     return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
 }
 
+// Two query tiles per CTA, two softmax warpgroups per tile (fwd3.cuh).
+template <int DQK>
+int launch3(const void* q, const void* k, const void* v, const FwdArgs& a, const Layout4& L,
+            cudaStream_t stream) {
+    using C = Fwd3Cfg<DQK>;
+    CUtensorMap tq, tk, tv;
+    const CUtensorMapSwizzle swz =
+        C::CB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!make_map(&tq, q, false, DQK, a.Hq, a.N, a.B, L.q, C::CB, swz)) return ZYFA_ERR_CUDA;
+    if (!make_map(&tk, k, false, DQK, a.Hkv, a.N, a.B, L.k, C::CB, swz)) return ZYFA_ERR_CUDA;
+    if (!make_map(&tv, v, false, C::DV, a.Hkv, a.N, a.B, L.v, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        return ZYFA_ERR_CUDA;
+    auto kern = zyfa_fwd3_kernel<DQK>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
+        cudaSuccess)
+        return ZYFA_ERR_CUDA;
+    const int T = a.N / C::BM;
+    const unsigned grid = static_cast<unsigned>(a.B) * a.Hq * ((T + 1) / 2);
+    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, a);
+    return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
+}
+
 template <bool FP8, int DQK, bool QK16 = !FP8>
 int launch(const void* q, const void* k, const void* v, const FwdArgs& a, const Layout4& L,
            cudaStream_t stream) {
@@ -191,11 +214,11 @@ extern "C" int zyfa_fwd_strided(const void* q, const void* k, const void* v,
     FwdArgs a{out, lse, descale_q, descale_k, descale_v, B, Hq, Hkv, N, p_mode, block_scale,
               causal, 1.0f / sqrtf(static_cast<float>(d_qk)), L.o.b, L.o.n, L.o.h};
     auto s = static_cast<cudaStream_t>(stream);
-    // Lean P at d_qk = 128: two query tiles per CTA (fwd2.cuh).  Exact P is
-    // bound by the ex2 unit, and at d_qk = 192 two Q tiles and double-buffered
-    // P leave shared memory for two K/V stages only; there one tile per CTA
-    // (fwd.cuh) measures faster.
-    if (p_mode == ZYFA_P_LEAN && d_qk == 128) return launch2<128>(q, k, v, a, L, s);
+    // Lean P at d_qk = 128: two query tiles per CTA with two softmax
+    // warpgroups per tile (fwd3.cuh).  Exact P is bound by the ex2 unit, and
+    // at d_qk = 192 two Q tiles and double-buffered P leave shared memory for
+    // two K/V stages only; there one tile per CTA (fwd.cuh) measures faster.
+    if (p_mode == ZYFA_P_LEAN && d_qk == 128) return launch3<128>(q, k, v, a, L, s);
     return d_qk == 128 ? launch<true, 128>(q, k, v, a, L, s) : launch<true, 192>(q, k, v, a, L, s);
 }
 
