@@ -57,7 +57,7 @@ struct FwdArgs {
     long long o_sb, o_sn, o_sh;    // element strides of out per batch, position, head
     // Key range [128 kb0, 128 kb1) in 128-key blocks: a call over part of the
     // keys, whose outputs are merged by their LSE (Sec. IV-B3).  The default
-    // is every key.  Only the one-tile kernel reads these.
+    // is every key.  Read by the kernels of fwd.cuh and fwd3.cuh.
     int kb0 = 0;
     int kb1 = 1 << 30;
 };

@@ -115,8 +115,15 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int qt0 = 2 * pair;                       // tile A; tile B = qt0 + 1
     const bool has_b = qt0 + 1 < T;
     // key blocks of each tile
-    const int nb0 = args.causal ? qt0 + 1 : T;
-    const int nb1 = has_b ? (args.causal ? qt0 + 2 : T) : 0;
+    // key blocks of each tile: kb0, kb0 + 1, ... up to the causal limit and
+    // the key range [128 kb0, 128 kb1) (a partial call; all keys otherwise)
+    auto nblocks = [&](int qt) {
+        const int lim = args.causal ? qt + 1 : T;
+        const int end = lim < args.kb1 ? lim : args.kb1;
+        return end > args.kb0 ? end - args.kb0 : 0;
+    };
+    const int nb0 = nblocks(qt0);
+    const int nb1 = has_b ? nblocks(qt0 + 1) : 0;
     const int nblk = nb0 > nb1 ? nb0 : nb1;
 
     if (threadIdx.x == 0) {
@@ -240,13 +247,13 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             #pragma unroll
             for (int c = 0; c < C::NCH; ++c)
                 tma_load_4d_elect(sbase + C::OFF_K + st * C::K_BYTES + c * (C::BN * C::CB), &tm_k,
-                                  BAR(B_KF + st), c * C::CB, g, i * C::BN, b);
+                                  BAR(B_KF + st), c * C::CB, g, (args.kb0 + i) * C::BN, b);
             mbar_expect_tx_elect(BAR(B_VF + st), C::V_BYTES);
             tma_load_4d_elect(sbase + C::OFF_V + st * C::V_BYTES, &tm_v, BAR(B_VF + st), 0, g,
-                              i * C::BN, b);
+                              (args.kb0 + i) * C::BN, b);
         };
         int li = 0;                                  // next K/V block to load (issuer A)
-        if (t == 0) {
+        if (t == 0 && nblk > 0) {                    // (nothing, not even Q, when no block)
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
@@ -406,7 +413,7 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             tc_fence_before();
             mbar_arrive(BAR(B_SX + t));
-            if (args.causal && j == qt) {                     // diagonal block: key > query
+            if (args.causal && args.kb0 + j == qt) {          // diagonal block: key > query
                 #pragma unroll
                 for (int k = 0; k < 64; ++k)
                     if (64 * hf + k > row) s[k] = -INFINITY;
@@ -533,6 +540,17 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                 }
             }
+        } else if (t == 0 || has_b) {
+            // no key of the range is visible to this tile: O = 0 and LSE =
+            // -inf, the identity of the merge
+            const long long orow = b * args.o_sb + (static_cast<long long>(qt) * C::BM + row) * args.o_sn +
+                                   h * args.o_sh;
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + orow + 64 * hf);
+            #pragma unroll
+            for (int k = 0; k < 8; ++k) dst[k] = make_uint4(0u, 0u, 0u, 0u);
+            if (args.lse && hf == 1)
+                args.lse[(static_cast<size_t>(b) * args.Hq + h) * args.N + static_cast<size_t>(qt) * C::BM + row] =
+                    -INFINITY;
         }
         tc_fence_before();
     }

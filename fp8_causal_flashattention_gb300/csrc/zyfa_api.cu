@@ -295,6 +295,8 @@ extern "C" int zyfa_fwd_partial(const void* q, const void* k, const void* v,
               causal, 1.0f / sqrtf(static_cast<float>(d_qk)), L.o.b, L.o.n, L.o.h,
               key_begin / 128, key_end / 128};
     auto s = static_cast<cudaStream_t>(stream);
+    // the kernels of zyfa_fwd_strided, which all read the key range
+    if (p_mode == ZYFA_P_LEAN && d_qk == 128) return launch3<128>(q, k, v, a, L, s);
     return d_qk == 128 ? launch<true, 128>(q, k, v, a, L, s) : launch<true, 192>(q, k, v, a, L, s);
 }
 

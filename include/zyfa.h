@@ -240,10 +240,10 @@ int zyfa_fwd_bf16qk_fp8pv(const void* q, const void* k, const void* v, const flo
  *   key_begin, key_end   multiples of 128, 0 <= key_begin <= key_end <= N
  *                        (ZYFA_ERR_SHAPE otherwise);
  *   lse                  required (ZYFA_ERR_NULL when NULL), FP32 [B, Hq, N].
- * Everything else as zyfa_fwd_strided (strides NULL for BSHD).  Always one
- * query tile per CTA.  Merging disjoint ranges that cover [0, N) gives
- * attention over all keys up to the BF16 rounding of each part and the
- * per-range choices of maximum and block scale.
+ * Everything else as zyfa_fwd_strided (strides NULL for BSHD), with the same
+ * kernels.  Merging disjoint ranges that cover [0, N) gives attention over
+ * all keys up to the BF16 rounding of each part and the per-range choices of
+ * maximum and block scale.
  */
 int zyfa_fwd_partial(const void* q, const void* k, const void* v,
                      const float* descale_q, const float* descale_k, const float* descale_v,

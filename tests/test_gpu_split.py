@@ -81,10 +81,10 @@ def test_key_range_matches_oracle(lib, case, mode):
         assert err.max() <= 2e-2 and np.sqrt(np.mean(err ** 2)) <= 5e-4, (kb, ke)
 
 
-@pytest.mark.parametrize("mode", ["exact", "bf16"])
+@pytest.mark.parametrize("mode", ["lean", "exact", "bf16"])
 def test_full_range_is_the_ordinary_call(lib, mode):
-    """Exact P and BF16 run the one-tile kernel either way: the range [0, N)
-    must give the ordinary call's output and LSE bit for bit."""
+    """A partial call runs the kernel the ordinary call runs: the range
+    [0, N) must give the ordinary call's output and LSE bit for bit."""
     import torch
     Z = lib
     wl, inp, dev = _inputs(("gqa", 2, 4, 2, 640, 128), mode, seed=12)
@@ -93,7 +93,8 @@ def test_full_range_is_the_ordinary_call(lib, mode):
     if mode == "bf16":
         ref, ref_lse = Z.attention_bf16(q, k, v, return_lse=True)
     else:
-        ref, ref_lse = Z.attention_fp8(q, k, v, ds[0], ds[1], ds[2], p_mode=Z.ZYFA_P_EXACT,
+        ref, ref_lse = Z.attention_fp8(q, k, v, ds[0], ds[1], ds[2],
+                                       p_mode=Z.ZYFA_P_LEAN if mode == "lean" else Z.ZYFA_P_EXACT,
                                        return_lse=True)
     assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
     assert torch.equal(lse, ref_lse)
