@@ -58,6 +58,24 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(ms: float, ws: int, device=None) -> float:
+    """The slowest rank's time: every rank's step time reduced with MAX (the
+    job is as fast as its slowest replica)."""
+    if ws <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(flops_per_rank: float, ws: int, ms: float) -> float:
+    """TFLOP/s of the whole job: the FLOPs all ranks processed over the
+    slowest rank's time."""
+    return flops_per_rank * ws / (ms * 1e-3) / 1e12
+
+
 def row_flops(wl: S.Workload, rows) -> float:
     i = np.asarray(rows) % wl.N
     return float(np.sum(2.0 * (i + 1) * (wl.d_qk + wl.d_v)))
@@ -251,15 +269,12 @@ def run_ours(args, wl: S.Workload):
     torch.cuda.synchronize()
     clocks = clk.stop()
     ms = e0.elapsed_time(e1) / args.steps
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, ws, dev)
     status = Z.zyfa_last_device_status()
     if status != Z.ZYFA_OK:
         raise RuntimeError(f"device status {status}")
     flops = wl.causal_flops
-    value = flops * ws / (ms * 1e-3) / 1e12
+    value = whole_job_value(flops, ws, ms)
 
     # end to end through the C ABI: pinned host inputs -> device, kernel,
     # output -> pinned host, every step
