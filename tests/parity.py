@@ -13,7 +13,7 @@ oracle on the same seeded inputs, and reports the errors:
 * ``snr_db`` against the running-maximum oracle (the paper's 30 dB gate,
   Sec. V-A).
 
-Gates (the benchmark spec): FP8 rel-L2 <= 1e-2 and max-abs <= 3e-2 max|V|; BF16
+Gates: FP8 rel-L2 <= 1e-2 and max-abs <= 3e-2 max|V|; BF16
 rel-L2 <= 5e-3.
 """
 from __future__ import annotations
