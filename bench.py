@@ -508,11 +508,55 @@ def run_sweep(args):
             abytes = wl.B * wl.N * (wl.Hq * wl.d_qk + wl.Hkv * (wl.d_qk + wl.d_v)) * (
                 2 if mode == "bf16" else 1) + wl.B * wl.N * wl.Hq * wl.d_v * 2
             hbm_roof = abytes / (ms * 1e-3) / 1e9
+            # the roof at this arithmetic intensity: min(tensor peak, AI x HBM)
+            roof = min(peak, wl.causal_flops / abytes * peaks["hbm_gbs"] * 1e9 / 1e12)
             print(json.dumps({"workload": name, "mode": mode, "tflops": tf, "ms": ms,
                               "frac_of_tensor_peak": tf / peak,
                               "algorithmic_GBps": hbm_roof,
                               "frac_of_hbm": hbm_roof / peaks["hbm_gbs"],
+                              "roof_tflops": roof, "frac_of_roof": tf / roof,
                               "sm_mhz": clocks.get("sm_mhz"), "reasons": clocks.get("reasons")}),
+                  flush=True)
+            del dev, inp
+            torch.cuda.empty_cache()
+
+
+def run_sustained(args):
+    """Sustained throughput: for the d=128 workload and the activation-like
+    GQA workload (the clock depends on the data), 1 s of warm-in, then three
+    back-to-back windows of at least 1 s each, CUDA-event timed, with the SM
+    clock sampled during each window.  One JSON line per workload and mode:
+    mean TFLOP/s, the spread over the three windows and the median clock."""
+    import torch
+    import fp8_causal_flashattention_gb300 as Z
+    from tests import parity as P
+    Z.load()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    for name in ("d128", "gqa_act"):
+        wl = S.WORKLOADS[name]
+        for mode in ("lean", "exact"):
+            inp = S.make_inputs(wl)
+            dev = P.to_device(inp, True)
+            run = lambda: P.gpu_run(inp, mode, dev)
+            one = time_launches(run, 3, 2, stream)           # ms per launch, to size the windows
+            n = max(3, int(1000.0 / one))                     # launches per ~1 s
+            time_launches(run, n, 0, stream)                  # 1 s warm-in
+            wins = []
+            for _ in range(3):
+                clk = ClockSampler(None)
+                clk.start()
+                ms = time_launches(run, n, 0, stream)
+                c = clk.stop()
+                wins.append((wl.causal_flops / (ms * 1e-3) / 1e12, c))
+            tfs = [w[0] for w in wins]
+            print(json.dumps({"workload": name, "mode": mode, "windows": 3,
+                              "seconds_per_window": n * one / 1000.0,
+                              "tflops_mean": float(np.mean(tfs)), "tflops_min": min(tfs),
+                              "tflops_max": max(tfs),
+                              "sm_mhz": [w[1].get("sm_mhz") for w in wins],
+                              "power_w_max": [w[1].get("power_w_max") for w in wins],
+                              "reasons": sorted({r for w in wins for r in w[1].get("reasons", [])})}),
                   flush=True)
             del dev, inp
             torch.cuda.empty_cache()
@@ -570,6 +614,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--sweep", action="store_true",
                     help="time every workload and mode (one JSON line each)")
+    ap.add_argument("--sustained", action="store_true",
+                    help="sustained throughput of the d128 and GQA workloads (3 x 1 s windows)")
     ap.add_argument("--accuracy", action="store_true",
                     help="error of one call on Fig. 15's synthetic inputs (one JSON line each)")
     args = ap.parse_args()
@@ -578,6 +624,9 @@ def main():
         return
     if args.accuracy:
         run_accuracy(args)
+        return
+    if args.sustained:
+        run_sustained(args)
         return
     wl = S.WORKLOADS[args.workload]
     if args.impl == "reference":
