@@ -34,6 +34,9 @@ def test_full_config_sampled_rows(lib, name):
         res = P.errors(got, inp, mode, rows, extra=True)
         print(name, mode, res, flush=True)
         assert P.passes(res, mode), (name, mode, res)
+        # the kernels compute the oracle's steps in FP32: held an order of
+        # magnitude inside the gate, as on the small all-rows cases
+        assert res["rel_l2"] <= 1e-3, (name, mode, res)
     if wl.kind == "activation":
         # the recipe: ~90% of visible (row, 64-key block) pairs > 8 binades down
         assert abs(inp.meta["far8_share"] - 0.90) <= 0.02
