@@ -111,8 +111,9 @@ int check_common(const void* q, const void* k, const void* v, void* out, int B, 
     return 1;   // proceed
 }
 
-// Two query tiles per CTA (fwd2.cuh), FP8 only: BF16 keeps one tile per CTA
-// (fwd.cuh), whose P stays in TMEM over the scores.
+// Two query tiles per CTA, one softmax warpgroup per tile (fwd2.cuh), FP8
+// only.  Not dispatched (never instantiated): fwd3.cuh replaced it for Lean P
+// at d_qk = 128.
 template <int DQK>
 int launch2(const void* q, const void* k, const void* v, const FwdArgs& a, const Layout4& L,
             cudaStream_t stream) {
