@@ -276,13 +276,24 @@ def run_ours(args, wl: S.Workload):
     flops = wl.causal_flops
     value = whole_job_value(flops, ws, ms)
 
-    # end to end through the C ABI: pinned host inputs -> device, kernel,
-    # output -> pinned host, every step
+    # end to end through the C ABI on host buffers, every step: zyfa_fwd_host
+    # copies the pinned inputs in, runs the kernels and copies the output
+    # back, pipelined over chunks of heads so that copies overlap kernels
     hq, hk, hv = (torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
                   for a in (inp.q8, inp.k8, inp.v8))
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    ws_bytes = Z.zyfa_fwd_host_workspace_bytes(wl.B, wl.Hq, wl.Hkv, wl.N, wl.d_qk, wl.d_v, 0)
+    work = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
 
     def e2e_step():
+        rc = Z.zyfa_fwd_host(hq, hk, hv, inp.descale, hout, None, wl.B, wl.Hq, wl.Hkv, wl.N,
+                             wl.d_qk, wl.d_v, 1, p_mode, bs, args.e2e_chunks, work, ws_bytes,
+                             stream)
+        if rc != Z.ZYFA_OK:
+            raise Z.ZyfaError(rc, "zyfa_fwd_host")
+
+    # the same without the pipeline: whole-tensor copies, kernel, copy back
+    def serial_step():
         q.copy_(hq, non_blocking=True)
         k.copy_(hk, non_blocking=True)
         v.copy_(hv, non_blocking=True)
@@ -290,9 +301,13 @@ def run_ours(args, wl: S.Workload):
         hout.copy_(out, non_blocking=True)
 
     e2e_steps = max(3, min(args.steps, 30))
-    e2e_ms = time_launches(e2e_step, e2e_steps, 2, stream)
+    e2e_ms = time_launches(e2e_step, e2e_steps, 3, stream)
+    serial_ms = time_launches(serial_step, e2e_steps, 2, stream)
+    if Z.zyfa_last_device_status() != Z.ZYFA_OK:
+        raise RuntimeError("device status after the end-to-end steps")
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = hout.numel() * hout.element_size()
+    del work
 
     peaks, peak_src = measured_peaks()
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
@@ -310,7 +325,10 @@ def run_ours(args, wl: S.Workload):
                                     f"{FP8_OVER_BF16} nominal FP8/BF16 ratio",
                      "algorithmic": "F = B*Hq*N^2*(d_qk+d_v) causal FLOPs per launch"},
         "e2e": {"value": flops * ws / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "call": "zyfa_fwd_host (pinned host buffers, copies pipelined over "
+                        f"n_chunks={args.e2e_chunks or 16} chunks of batch elements or heads)",
+                "serial_ms_per_step": serial_ms},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "kernel_hash": kernel_hash(),
@@ -609,6 +627,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="d128", choices=sorted(S.WORKLOADS))
     ap.add_argument("--mode", default="lean", choices=["lean", "exact", "lean_nobs", "exact_nobs"])
+    ap.add_argument("--e2e-chunks", type=int, default=0,
+                    help="n_chunks of the end-to-end host call (0: the library's choice)")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)

@@ -32,6 +32,7 @@ ZYFA_P_LEAN = 1
 EXPORTS = ("zyfa_fwd", "zyfa_fwd_bf16", "zyfa_fwd_ex", "zyfa_fwd_bf16_ex",
            "zyfa_fwd_strided", "zyfa_fwd_bf16_strided", "zyfa_fwd_bf16qk_fp8pv",
            "zyfa_fwd_partial", "zyfa_fwd_bf16_partial", "zyfa_merge",
+           "zyfa_fwd_host", "zyfa_fwd_host_workspace_bytes",
            "zyfa_quantize", "zyfa_quantize_noalloc", "zyfa_status_string", "zyfa_last_device_status", "zyfa_selftest_timeout",
            "zyfa_version")
 
@@ -76,6 +77,10 @@ def load():
     lib.zyfa_fwd_bf16_partial.restype = ci
     lib.zyfa_merge.argtypes = [vp, vp, ci, vp, vp] + [ci] * 4 + [vp]
     lib.zyfa_merge.restype = ci
+    lib.zyfa_fwd_host.argtypes = [vp] * 6 + [ci] * 10 + [vp, ctypes.c_size_t, vp]
+    lib.zyfa_fwd_host.restype = ci
+    lib.zyfa_fwd_host_workspace_bytes.argtypes = [ci] * 7
+    lib.zyfa_fwd_host_workspace_bytes.restype = ctypes.c_size_t
     lib.zyfa_quantize.argtypes = [vp, vp, ci, ctypes.c_float, vp, vp, vp] + [ci] * 4 + [vp]
     lib.zyfa_quantize_noalloc.restype = ci
     lib.zyfa_quantize_noalloc.argtypes = lib.zyfa_quantize.argtypes
@@ -92,7 +97,7 @@ def load():
 
 
 def _ptr(x):
-    """Device address of a tensor (or an int / None passed through)."""
+    """Address of a tensor's data (or an int / None passed through)."""
     if x is None:
         return None
     if isinstance(x, int):
@@ -227,6 +232,24 @@ def zyfa_merge(outs, lses, out, lse, B, Hq, N, d_v, stream=None) -> int:
                              n, _ptr(out), _ptr(lse), B, Hq, N, d_v, _stream(stream))
 
 
+def zyfa_fwd_host(q, k, v, descale, out, lse, B, Hq, Hkv, N, d_qk, d_v, causal=1,
+                  p_mode=ZYFA_P_LEAN, block_scale=1, n_chunks=0, workspace=None,
+                  workspace_bytes=0, stream=None) -> int:
+    """``zyfa_fwd_host`` of include/zyfa.h: q, k, v, out, lse are HOST tensors
+    (or host addresses), ``descale`` a sequence of three floats or None,
+    ``workspace`` a device tensor or address."""
+    ds = None if descale is None else (ctypes.c_float * 3)(*[float(x) for x in descale])
+    return load().zyfa_fwd_host(_ptr(q), _ptr(k), _ptr(v),
+                                None if ds is None else ctypes.cast(ds, ctypes.c_void_p),
+                                _ptr(out), _ptr(lse), B, Hq, Hkv, N, d_qk, d_v, causal, p_mode,
+                                block_scale, n_chunks, _ptr(workspace), workspace_bytes,
+                                _stream(stream))
+
+
+def zyfa_fwd_host_workspace_bytes(B, Hq, Hkv, N, d_qk, d_v, with_lse) -> int:
+    return load().zyfa_fwd_host_workspace_bytes(B, Hq, Hkv, N, d_qk, d_v, 1 if with_lse else 0)
+
+
 def zyfa_status_string(status: int) -> str:
     return load().zyfa_status_string(int(status)).decode()
 
@@ -284,6 +307,54 @@ def attention_fp8(q, k, v, descale_q=None, descale_k=None, descale_v=None, *,
     if rc != ZYFA_OK:
         raise ZyfaError(rc, "zyfa_fwd_strided")
     return (out, lse) if return_lse else out
+
+
+def host_workspace(q, k, v, *, with_lse=False, device=None):
+    """A device workspace (uint8 tensor) large enough for attention_fp8_host
+    on tensors shaped like q, k, v."""
+    import torch
+    B, N, Hq, Hkv, d_qk, d_v = _shape(q, k, v)
+    n = zyfa_fwd_host_workspace_bytes(B, Hq, Hkv, N, d_qk, d_v, with_lse)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device or "cuda")
+
+
+def attention_fp8_host(q, k, v, descale=None, *, p_mode=ZYFA_P_LEAN, block_scale=1, causal=1,
+                       out=None, return_lse=False, lse=None, workspace=None, n_chunks=0,
+                       sync=True, stream=None):
+    """Causal FP8 attention on HOST tensors, end to end in one call
+    (``zyfa_fwd_host``): copies in, kernels and copies out pipelined over
+    chunks of batch elements or heads.  q, k, v: CPU tensors, contiguous
+    BSHD, e4m3 codes (torch.float8_e4m3fn or uint8), page-locked for the
+    copies to overlap; ``descale``: three floats (q, k, v) or None;
+    ``workspace``: a CUDA uint8 tensor (host_workspace), or None to allocate
+    one.  Returns the host BF16 output (and the FP32 LSE [B, Hq, N]); with
+    ``sync=False`` they are complete only once ``stream`` has been
+    synchronised."""
+    import torch
+    B, N, Hq, Hkv, d_qk, d_v = _shape(q, k, v)
+    for t in (q, k, v):
+        if t.device.type != "cpu" or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous CPU tensors")
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty((B, N, Hq, d_v), dtype=torch.bfloat16, pin_memory=pin)
+    if return_lse and lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, pin_memory=pin)
+    if workspace is None:
+        workspace = host_workspace(q, k, v, with_lse=lse is not None)
+    nbytes = workspace.numel() * workspace.element_size()
+    rc = zyfa_fwd_host(q, k, v, descale, out, lse, B, Hq, Hkv, N, d_qk, d_v, causal, p_mode,
+                       block_scale, n_chunks, workspace, nbytes, stream)
+    if rc != ZYFA_OK:
+        raise ZyfaError(rc, "zyfa_fwd_host")
+    if sync:
+        if stream is None:
+            torch.cuda.current_stream().synchronize()
+        elif isinstance(stream, int):
+            torch.cuda.synchronize()
+        else:
+            stream.synchronize()
+    return (out, lse) if lse is not None else out
 
 
 def attention_bf16(q, k, v, *, causal=1, out=None, return_lse=False, stream=None):

@@ -348,7 +348,7 @@ extern "C" const char* zyfa_status_string(int status) {
         case ZYFA_ERR_ALIGN: return "misaligned pointer (tensors need 16 bytes, scales 4)";
         case ZYFA_ERR_CUDA: return "CUDA launch or driver call failed";
         case ZYFA_ERR_TIMEOUT: return "a device-side wait ran out of time";
-        case ZYFA_ERR_SCRATCH: return "the call needs more scratch than the no-alloc buffer holds";
+        case ZYFA_ERR_SCRATCH: return "the call needs more scratch (no-alloc buffer) or workspace than it has";
         default: return "unknown status";
     }
 }

@@ -27,9 +27,11 @@
  *   - Supported: causal = 1 (the paper's setting) or 0 (every query sees
  *     every key); N a multiple of 128; (d_qk, d_v) = (128, 128) or
  *     (192, 128); Hq a multiple of Hkv.
- *   - Ownership: every buffer is device memory owned by the caller.  The
+ *   - Ownership: every buffer is device memory owned by the caller (but
+ *     zyfa_fwd_host, which takes host buffers and a device workspace).  The
  *     attention entry points allocate no device memory, keep no pointer
- *     after the call returns and write nothing but `out` (and `lse`).
+ *     after the call returns and write nothing but `out` (and `lse`, and
+ *     zyfa_fwd_host's workspace).
  *     zyfa_quantize takes stream-ordered scratch (cudaMallocAsync /
  *     cudaFreeAsync on `stream`) when it needs a per-call maximum or a mean.
  *   - Asynchrony: work is enqueued on `stream` (a cudaStream_t; NULL is the
@@ -44,6 +46,8 @@
 #ifndef ZYFA_H
 #define ZYFA_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -56,7 +60,7 @@ typedef enum {
     ZYFA_ERR_ALIGN = -4,        /* a tensor not 16-byte aligned, a scale not 4    */
     ZYFA_ERR_CUDA = -5,         /* launch or driver call failed                   */
     ZYFA_ERR_TIMEOUT = -6,      /* a device-side wait ran out (see below)         */
-    ZYFA_ERR_SCRATCH = -7       /* needs more than zyfa_quantize_noalloc's buffer */
+    ZYFA_ERR_SCRATCH = -7       /* needs more scratch or workspace than given      */
 } zyfa_status;
 
 enum { ZYFA_P_EXACT = 0, ZYFA_P_LEAN = 1 };
@@ -274,6 +278,55 @@ int zyfa_fwd_bf16_partial(const void* q, const void* k, const void* v, void* out
  */
 int zyfa_merge(const void* const* outs, const float* const* lses, int n_parts, void* out,
                float* lse, int B, int Hq, int N, int d_v, void* stream);
+
+/*
+ * The FP8 forward end to end on HOST buffers: the inputs are copied to
+ * device memory, zyfa_fwd_strided's kernels run, and the output (and the
+ * LSE) are copied back.  Attention is independent per batch element and per
+ * key/value head with its query heads (Sec. II-B; Table VI's grouped-query
+ * shapes), so the work is cut into chunks whose copies overlap the other
+ * chunks' kernels: ranges of batch elements with all heads when
+ * B >= n_chunks, else each batch element's key/value heads split into the
+ * largest number of equal groups not above ceil(n_chunks / B).  The result
+ * is bit-identical to zyfa_fwd_ex on the same data.
+ *   q, k, v      HOST e4m3 codes, contiguous BSHD as zyfa_fwd.  Page-locked
+ *                memory (cudaHostAlloc / cudaHostRegister) lets the copies
+ *                overlap the kernels; pageable memory also works, but the
+ *                copies then block the host and do not overlap.
+ *   descale      HOST array {descale_q, descale_k, descale_v}, read during
+ *                the call (the values are passed to the device by value),
+ *                or NULL for 1.0 each.
+ *   out          HOST BF16 [B, N, Hq, d_v];  lse  HOST FP32 [B, Hq, N] or
+ *                NULL.  Both are written when the work enqueued on `stream`
+ *                completes (synchronise `stream` before reading them).
+ *   n_chunks     0 (the library's choice, 16) or 1 .. 32 (ZYFA_ERR_SHAPE
+ *                otherwise); the plan holds at most 2 x n_chunks - 1 chunks.
+ *   workspace    device memory owned by the caller, 256-byte aligned
+ *                (ZYFA_ERR_ALIGN), of at least
+ *                zyfa_fwd_host_workspace_bytes(B, Hq, Hkv, N, d_qk, d_v,
+ *                lse != NULL) bytes (ZYFA_ERR_SCRATCH when smaller): the
+ *                device copies of q, k, v, out and lse and the three scales.
+ *                It must not be used by other work until `stream` has passed
+ *                the call.
+ * Everything else (shapes, modes, errors) as zyfa_fwd_ex; every argument
+ * error is returned before anything is enqueued.  The work runs on four
+ * streams the library keeps per device (created on the first call and kept
+ * for the life of the process), forked from `stream` and joined back to it
+ * with events, so the call is ordered on `stream` like the other entry
+ * points and can be captured into a CUDA graph (page-locked buffers only).
+ * Calls from several host threads take a lock while they enqueue.  A copy
+ * or launch that fails returns ZYFA_ERR_CUDA after the streams are joined.
+ */
+int zyfa_fwd_host(const void* q, const void* k, const void* v, const float* descale, void* out,
+                  float* lse, int B, int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
+                  int p_mode, int block_scale, int n_chunks, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
+/* Device bytes zyfa_fwd_host needs as workspace (the device copies rounded
+ * up to 256 bytes each, plus 256 for the scales); 0 for negative sizes, Hq
+ * or Hkv below 1, or a total beyond 2^63.  Pure host arithmetic. */
+size_t zyfa_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int N, int d_qk, int d_v,
+                                     int with_lse);
 
 /* Static, NUL-terminated description of a status code. */
 const char* zyfa_status_string(int status);

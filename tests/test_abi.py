@@ -198,3 +198,66 @@ def test_merge_argument_errors(lib, kw, want):
 def test_merge_empty_problem_is_ok(lib):
     assert Z.zyfa_merge([FAKE], [FAKE], FAKE, None, 0, 2, 256, 128, stream=0) == Z.ZYFA_OK
     assert Z.zyfa_merge([FAKE], [FAKE], FAKE, None, 1, 2, 0, 128, stream=0) == Z.ZYFA_OK
+
+
+def _r256(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,N,dqk,dv,lse", [
+    (1, 32, 32, 32768, 128, 128, 0), (2, 8, 2, 384, 192, 128, 1), (3, 6, 3, 128, 128, 128, 1),
+    (0, 4, 4, 256, 128, 128, 1), (1, 1, 1, 0, 128, 128, 0)])
+def test_host_workspace_bytes(lib, B, Hq, Hkv, N, dqk, dv, lse):
+    bn = B * N
+    want = (_r256(bn * Hq * dqk) + _r256(bn * Hkv * dqk) + _r256(bn * Hkv * dv) +
+            _r256(bn * Hq * dv * 2) + (_r256(bn * Hq * 4) if lse else 0) + 256)
+    assert Z.zyfa_fwd_host_workspace_bytes(B, Hq, Hkv, N, dqk, dv, lse) == want
+
+
+@pytest.mark.parametrize("bad", [dict(B=-1), dict(Hq=0), dict(Hkv=0), dict(N=-128)])
+def test_host_workspace_bytes_rejects(lib, bad):
+    a = dict(B=1, Hq=4, Hkv=4, N=256, d_qk=128, d_v=128)
+    a.update(bad)
+    assert Z.zyfa_fwd_host_workspace_bytes(a["B"], a["Hq"], a["Hkv"], a["N"], a["d_qk"],
+                                           a["d_v"], 0) == 0
+
+
+HOST = 0x10000                                 # never dereferenced: every case fails first
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(B=-1), Z.ZYFA_ERR_SHAPE),
+    (dict(Hkv=3), Z.ZYFA_ERR_SHAPE),                     # Hq % Hkv
+    (dict(N=200), Z.ZYFA_ERR_SHAPE),
+    (dict(causal=2), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(d_qk=64), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(p_mode=7), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(block_scale=2), Z.ZYFA_ERR_UNSUPPORTED),
+    (dict(n_chunks=-1), Z.ZYFA_ERR_SHAPE),
+    (dict(n_chunks=33), Z.ZYFA_ERR_SHAPE),
+    (dict(q=None), Z.ZYFA_ERR_NULL),
+    (dict(out=None), Z.ZYFA_ERR_NULL),
+    (dict(workspace=None), Z.ZYFA_ERR_NULL),
+    (dict(workspace=FAKE + 16), Z.ZYFA_ERR_ALIGN),       # 256-byte alignment
+    (dict(workspace_bytes=-1), Z.ZYFA_ERR_SCRATCH),      # one byte short
+    (dict(lse=HOST, workspace_bytes=0), Z.ZYFA_ERR_SCRATCH),   # the LSE needs room too
+    (dict(B=1 << 20, N=1 << 16, Hq=8, Hkv=8), Z.ZYFA_ERR_SHAPE),   # B Hq N/128 >= 2^31
+])
+def test_host_argument_errors(lib, kw, want):
+    a = dict(q=HOST, k=HOST, v=HOST, descale=None, out=HOST, lse=None, B=1, Hq=4, Hkv=2, N=256,
+             d_qk=128, d_v=128, causal=1, p_mode=Z.ZYFA_P_LEAN, block_scale=1, n_chunks=0,
+             workspace=FAKE, workspace_bytes=0)
+    a.update(kw)
+    if a["workspace_bytes"] <= 0:                # relative to what the shape needs
+        a["workspace_bytes"] += Z.zyfa_fwd_host_workspace_bytes(
+            a["B"], a["Hq"], a["Hkv"], a["N"], a["d_qk"], a["d_v"], 0)
+    assert Z.zyfa_fwd_host(a["q"], a["k"], a["v"], a["descale"], a["out"], a["lse"], a["B"],
+                           a["Hq"], a["Hkv"], a["N"], a["d_qk"], a["d_v"], a["causal"],
+                           a["p_mode"], a["block_scale"], a["n_chunks"], a["workspace"],
+                           a["workspace_bytes"], stream=0) == want
+
+
+def test_host_empty_problem_is_ok(lib):
+    for B, N in ((0, 256), (1, 0)):
+        assert Z.zyfa_fwd_host(None, None, None, None, None, None, B, 4, 2, N, 128, 128, 1,
+                               Z.ZYFA_P_LEAN, 1, 0, None, 0, stream=0) == Z.ZYFA_OK
