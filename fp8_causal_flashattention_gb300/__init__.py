@@ -32,7 +32,7 @@ ZYFA_P_LEAN = 1
 EXPORTS = ("zyfa_fwd", "zyfa_fwd_bf16", "zyfa_fwd_ex", "zyfa_fwd_bf16_ex",
            "zyfa_fwd_strided", "zyfa_fwd_bf16_strided", "zyfa_fwd_bf16qk_fp8pv",
            "zyfa_fwd_partial", "zyfa_fwd_bf16_partial", "zyfa_merge",
-           "zyfa_fwd_host", "zyfa_fwd_host_workspace_bytes",
+           "zyfa_fwd_host", "zyfa_fwd_host_workspace_bytes", "zyfa_fwd_host_plan",
            "zyfa_quantize", "zyfa_quantize_noalloc", "zyfa_status_string", "zyfa_last_device_status", "zyfa_selftest_timeout",
            "zyfa_version")
 
@@ -81,6 +81,8 @@ def load():
     lib.zyfa_fwd_host.restype = ci
     lib.zyfa_fwd_host_workspace_bytes.argtypes = [ci] * 7
     lib.zyfa_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.zyfa_fwd_host_plan.argtypes = [ci] * 4 + [vp, ci]
+    lib.zyfa_fwd_host_plan.restype = ci
     lib.zyfa_quantize.argtypes = [vp, vp, ci, ctypes.c_float, vp, vp, vp] + [ci] * 4 + [vp]
     lib.zyfa_quantize_noalloc.restype = ci
     lib.zyfa_quantize_noalloc.argtypes = lib.zyfa_quantize.argtypes
@@ -248,6 +250,18 @@ def zyfa_fwd_host(q, k, v, descale, out, lse, B, Hq, Hkv, N, d_qk, d_v, causal=1
 
 def zyfa_fwd_host_workspace_bytes(B, Hq, Hkv, N, d_qk, d_v, with_lse) -> int:
     return load().zyfa_fwd_host_workspace_bytes(B, Hq, Hkv, N, d_qk, d_v, 1 if with_lse else 0)
+
+
+def zyfa_fwd_host_plan(B, Hq, Hkv, n_chunks=0):
+    """``zyfa_fwd_host_plan`` of include/zyfa.h: the chunk list as tuples
+    (b0, nb, g0, hk, h0, hq, kv), or a negative status."""
+    lib = load()
+    m = lib.zyfa_fwd_host_plan(B, Hq, Hkv, n_chunks, None, 0)
+    if m < 0:
+        return m
+    buf = (ctypes.c_int * max(7 * m, 1))()
+    lib.zyfa_fwd_host_plan(B, Hq, Hkv, n_chunks, ctypes.cast(buf, ctypes.c_void_p), m)
+    return [tuple(buf[7 * c:7 * c + 7]) for c in range(m)]
 
 
 def zyfa_status_string(status: int) -> str:

@@ -52,31 +52,51 @@ bool carve(int B, int Hq, int Hkv, int N, int d_qk, int d_v, bool with_lse, Carv
     return true;
 }
 
-// One chunk: batch elements [b0, b0 + nb) and key/value heads
-// [g0, g0 + hk) (with query heads [g0 * G, (g0 + hk) * G), G = Hq / Hkv).
+// One chunk: batch elements [b0, b0 + nb), key/value heads [g0, g0 + hk)
+// and query heads [h0, h0 + hq) of those key/value heads; kv = 1 when the
+// chunk copies its K and V in (0: an earlier chunk of the same key/value
+// head already did).
 struct Chunk {
-    int b0, nb, g0, hk;
+    int b0, nb, g0, hk, h0, hq, kv;
 };
 
-int plan(int B, int Hkv, int n, Chunk* out) {
+int largest_divisor_upto(int x, int cap) {
+    int d = 1;
+    for (int g = 1; g <= cap && g <= x; ++g)
+        if (x % g == 0) d = g;
+    return d;
+}
+
+int plan(int B, int Hq, int Hkv, int n, Chunk* out) {
+    const int G = Hq / Hkv;
     if (B >= n) {                                    // ranges of whole batch elements
         for (int c = 0; c < n; ++c) {
             const int b0 = static_cast<int>(static_cast<long long>(c) * B / n);
             const int b1 = static_cast<int>(static_cast<long long>(c + 1) * B / n);
-            out[c] = {b0, b1 - b0, 0, Hkv};
+            out[c] = {b0, b1 - b0, 0, Hkv, 0, Hq, 1};
         }
         return n;
     }
-    // fewer batch elements than chunks: split each one's heads into the
-    // largest number of equal groups that does not exceed ceil(n / B)
-    const int want = (n + B - 1) / B;
-    int groups = 1;
-    for (int g = 1; g <= want && g <= Hkv; ++g)
-        if (Hkv % g == 0) groups = g;
-    const int hk = Hkv / groups;
+    const int want = (n + B - 1) / B;                // chunks per batch element
     int m = 0;
+    if (Hkv >= want) {
+        // groups of whole key/value heads: the largest number of equal
+        // groups that does not exceed ceil(n / B)
+        const int groups = largest_divisor_upto(Hkv, want);
+        const int hk = Hkv / groups;
+        for (int b = 0; b < B; ++b)
+            for (int g = 0; g < groups; ++g) out[m++] = {b, 1, g * hk, hk, g * hk * G, hk * G, 1};
+        return m;
+    }
+    // fewer key/value heads than wanted chunks (one K/V head shared by many
+    // query heads, e.g. Hkv = 1): one key/value head per chunk group, its
+    // query heads split into equal sub-ranges; the first sub-range copies
+    // the head's K and V, the others reuse them
+    const int sub = largest_divisor_upto(G, (want + Hkv - 1) / Hkv);
+    const int qs = G / sub;
     for (int b = 0; b < B; ++b)
-        for (int g = 0; g < groups; ++g) out[m++] = {b, 1, g * hk, hk};
+        for (int g = 0; g < Hkv; ++g)
+            for (int u = 0; u < sub; ++u) out[m++] = {b, 1, g, 1, g * G + u * qs, qs, u == 0};
     return m;
 }
 
@@ -130,6 +150,19 @@ bool copy_rows(void* dst, size_t dpitch, const void* src, size_t spitch, size_t 
 
 }  // namespace
 
+extern "C" int zyfa_fwd_host_plan(int B, int Hq, int Hkv, int n_chunks, int* chunks, int cap) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return ZYFA_ERR_SHAPE;
+    if (n_chunks < 0 || n_chunks > kMaxChunks || cap < 0) return ZYFA_ERR_SHAPE;
+    if (cap > 0 && !chunks) return ZYFA_ERR_NULL;
+    Chunk ch[kMaxPlan];
+    const int m = plan(B, Hq, Hkv, n_chunks ? n_chunks : kDefaultChunks, ch);
+    for (int c = 0; c < m && c < cap; ++c) {
+        const int v[7] = {ch[c].b0, ch[c].nb, ch[c].g0, ch[c].hk, ch[c].h0, ch[c].hq, ch[c].kv};
+        for (int i = 0; i < 7; ++i) chunks[7 * c + i] = v[i];
+    }
+    return m;
+}
+
 extern "C" size_t zyfa_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int N, int d_qk,
                                                 int d_v, int with_lse) {
     Carve c;
@@ -157,7 +190,7 @@ extern "C" int zyfa_fwd_host(const void* q, const void* k, const void* v, const 
     if (workspace_bytes < cv.total) return ZYFA_ERR_SCRATCH;
 
     Chunk ch[kMaxPlan];
-    const int m = plan(B, Hkv, n_chunks ? n_chunks : kDefaultChunks, ch);
+    const int m = plan(B, Hq, Hkv, n_chunks ? n_chunks : kDefaultChunks, ch);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return ZYFA_ERR_CUDA;
     std::lock_guard<std::mutex> guard(g_lock);
@@ -177,7 +210,6 @@ extern "C" int zyfa_fwd_host(const void* q, const void* k, const void* v, const 
     for (cudaStream_t s : lane)
         if (cudaStreamWaitEvent(s, L->fork, 0) != cudaSuccess) rc = ZYFA_ERR_CUDA;
 
-    const int G = Hq / Hkv;
     const size_t qrow = static_cast<size_t>(Hq) * d_qk;        // bytes per (b, n) row
     const size_t krow = static_cast<size_t>(Hkv) * d_qk;
     const size_t vrow = static_cast<size_t>(Hkv) * d_v;
@@ -196,19 +228,23 @@ extern "C" int zyfa_fwd_host(const void* q, const void* k, const void* v, const 
         const Chunk& x = ch[c];
         const size_t r0 = static_cast<size_t>(x.b0) * N;     // first (b, n) row
         const size_t rows = static_cast<size_t>(x.nb) * N;
-        const int h0 = x.g0 * G, hq = x.hk * G;              // query heads of the chunk
+        const int h0 = x.h0, hq = x.hq;                      // query heads of the chunk
         const size_t oq = r0 * qrow + static_cast<size_t>(h0) * d_qk;
         const size_t okk = r0 * krow + static_cast<size_t>(x.g0) * d_qk;
         const size_t ov = r0 * vrow + static_cast<size_t>(x.g0) * d_v;
         const size_t oo = r0 * orow + static_cast<size_t>(h0) * d_v * 2;
         const size_t ol = (static_cast<size_t>(x.b0) * Hq + h0) * N;    // LSE element
         cudaStream_t ks = L->kern[c & 1];
+        // copies in, in plan order on one stream: a chunk that reuses K and V
+        // is ordered after the chunk that copied them
         if (!copy_rows(ws + cv.q + oq, qrow, hq8 + oq, qrow, static_cast<size_t>(hq) * d_qk, rows,
                        cudaMemcpyHostToDevice, L->in) ||
-            !copy_rows(ws + cv.k + okk, krow, hk8 + okk, krow, static_cast<size_t>(x.hk) * d_qk,
-                       rows, cudaMemcpyHostToDevice, L->in) ||
-            !copy_rows(ws + cv.v + ov, vrow, hv8 + ov, vrow, static_cast<size_t>(x.hk) * d_v, rows,
-                       cudaMemcpyHostToDevice, L->in) ||
+            (x.kv && !copy_rows(ws + cv.k + okk, krow, hk8 + okk, krow,
+                                static_cast<size_t>(x.hk) * d_qk, rows, cudaMemcpyHostToDevice,
+                                L->in)) ||
+            (x.kv && !copy_rows(ws + cv.v + ov, vrow, hv8 + ov, vrow,
+                                static_cast<size_t>(x.hk) * d_v, rows, cudaMemcpyHostToDevice,
+                                L->in)) ||
             cudaEventRecord(L->in_done[c], L->in) != cudaSuccess ||
             cudaStreamWaitEvent(ks, L->in_done[c], 0) != cudaSuccess) {
             rc = ZYFA_ERR_CUDA;

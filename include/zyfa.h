@@ -283,12 +283,15 @@ int zyfa_merge(const void* const* outs, const float* const* lses, int n_parts, v
  * The FP8 forward end to end on HOST buffers: the inputs are copied to
  * device memory, zyfa_fwd_strided's kernels run, and the output (and the
  * LSE) are copied back.  Attention is independent per batch element and per
- * key/value head with its query heads (Sec. II-B; Table VI's grouped-query
- * shapes), so the work is cut into chunks whose copies overlap the other
- * chunks' kernels: ranges of batch elements with all heads when
- * B >= n_chunks, else each batch element's key/value heads split into the
- * largest number of equal groups not above ceil(n_chunks / B).  The result
- * is bit-identical to zyfa_fwd_ex on the same data.
+ * query head (Sec. II-B; a key/value head serves Hq / Hkv query heads,
+ * Table VI), so the work is cut into chunks whose copies overlap the other
+ * chunks' kernels (zyfa_fwd_host_plan): ranges of batch elements with all
+ * heads when B >= n_chunks; else, with w = ceil(n_chunks / B) chunks per
+ * batch element, its key/value heads in the largest number of equal groups
+ * not above w when Hkv >= w, or else one key/value head per chunk group
+ * with its query heads split into the largest number of equal sub-ranges
+ * not above ceil(w / Hkv) (K and V copied once, by the first sub-range).
+ * The result is bit-identical to zyfa_fwd_ex on the same data.
  *   q, k, v      HOST e4m3 codes, contiguous BSHD as zyfa_fwd.  Page-locked
  *                memory (cudaHostAlloc / cudaHostRegister) lets the copies
  *                overlap the kernels; pageable memory also works, but the
@@ -321,6 +324,16 @@ int zyfa_fwd_host(const void* q, const void* k, const void* v, const float* desc
                   float* lse, int B, int Hq, int Hkv, int N, int d_qk, int d_v, int causal,
                   int p_mode, int block_scale, int n_chunks, void* workspace,
                   size_t workspace_bytes, void* stream);
+
+/* The chunk plan zyfa_fwd_host follows, as pure host arithmetic (no CUDA
+ * call): writes the first `cap` chunks as 7 ints each, {b0, nb, g0, hk, h0,
+ * hq, kv}: batch elements [b0, b0 + nb), key/value heads [g0, g0 + hk),
+ * query heads [h0, h0 + hq), kv = 1 when the chunk copies K and V in (0:
+ * an earlier chunk copied them).  Returns the number of chunks (at most
+ * 2 x n_chunks - 1; n_chunks = 0 means 16), or ZYFA_ERR_SHAPE (B, Hq or
+ * Hkv below 1, Hq % Hkv, n_chunks outside 0 .. 32, cap < 0) or
+ * ZYFA_ERR_NULL (chunks NULL with cap > 0). */
+int zyfa_fwd_host_plan(int B, int Hq, int Hkv, int n_chunks, int* chunks, int cap);
 
 /* Device bytes zyfa_fwd_host needs as workspace (the device copies rounded
  * up to 256 bytes each, plus 256 for the scales); 0 for negative sizes, Hq

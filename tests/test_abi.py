@@ -261,3 +261,55 @@ def test_host_empty_problem_is_ok(lib):
     for B, N in ((0, 256), (1, 0)):
         assert Z.zyfa_fwd_host(None, None, None, None, None, None, B, 4, 2, N, 128, 128, 1,
                                Z.ZYFA_P_LEAN, 1, 0, None, 0, stream=0) == Z.ZYFA_OK
+
+
+def _check_plan(B, Hq, Hkv, n):
+    G = Hq // Hkv
+    plan = Z.zyfa_fwd_host_plan(B, Hq, Hkv, n)
+    assert isinstance(plan, list) and 1 <= len(plan) <= max(2 * (n or 16) - 1, 1)
+    seen = {}
+    copied = set()
+    for c, (b0, nb, g0, hk, h0, hq, kv) in enumerate(plan):
+        assert nb >= 1 and hk >= 1 and hq >= 1 and hq % hk == 0
+        assert 0 <= b0 and b0 + nb <= B and 0 <= g0 and g0 + hk <= Hkv
+        assert 0 <= h0 and h0 + hq <= Hq
+        r = hq // hk
+        for hl in range(hq):
+            # the kernel's view maps local query head hl to local K/V head
+            # hl // (hq / hk): it must be the global head's own K/V head
+            assert (h0 + hl) // G == g0 + hl // r
+        for b in range(b0, b0 + nb):
+            for g in range(g0, g0 + hk):
+                if kv:
+                    assert (b, g) not in copied
+                    copied.add((b, g))
+                else:
+                    assert (b, g) in copied              # copied by an earlier chunk
+            for h in range(h0, h0 + hq):
+                assert (b, h) not in seen
+                seen[(b, h)] = c
+    assert len(seen) == B * Hq and len(copied) == B * Hkv
+
+
+@pytest.mark.parametrize("B,Hq,Hkv", [
+    (1, 32, 32), (1, 32, 8), (1, 32, 1), (2, 32, 8), (3, 8, 2), (1, 128, 128), (1, 7, 7),
+    (1, 64, 2), (4, 32, 32), (5, 12, 3), (17, 4, 4), (1, 1, 1), (2, 6, 1), (1, 96, 3)])
+@pytest.mark.parametrize("n", [0, 1, 2, 3, 4, 7, 8, 16, 31, 32])
+def test_host_plan_partitions_the_problem(lib, B, Hq, Hkv, n):
+    _check_plan(B, Hq, Hkv, n)
+
+
+def test_host_plan_shapes_used_by_the_bench(lib):
+    # B=1, 32 heads, 16 chunks of 2 heads; one K/V head: query sub-ranges
+    assert [c[5] for c in Z.zyfa_fwd_host_plan(1, 32, 32, 16)] == [2] * 16
+    p = Z.zyfa_fwd_host_plan(1, 32, 1, 16)
+    assert [c[4] for c in p] == list(range(0, 32, 2)) and [c[6] for c in p] == [1] + [0] * 15
+
+
+@pytest.mark.parametrize("args,want", [
+    ((0, 4, 4, 0), Z.ZYFA_ERR_SHAPE), ((1, 0, 1, 0), Z.ZYFA_ERR_SHAPE),
+    ((1, 6, 4, 0), Z.ZYFA_ERR_SHAPE), ((1, 4, 4, -1), Z.ZYFA_ERR_SHAPE),
+    ((1, 4, 4, 33), Z.ZYFA_ERR_SHAPE)])
+def test_host_plan_errors(lib, args, want):
+    assert Z.zyfa_fwd_host_plan(*args) == want
+    assert Z.load().zyfa_fwd_host_plan(1, 4, 4, 0, None, 3) == Z.ZYFA_ERR_NULL

@@ -14,7 +14,8 @@ pytestmark = pytest.mark.gpu
 
 # (B, Hq, Hkv, N, d_qk, mode, n_chunks): plans of one chunk, batch ranges,
 # head groups (with and without grouped-query heads), a group count that is
-# not a divisor (3 of 8 heads -> 2 groups), more chunks than heads, d_qk=192
+# not a divisor (3 of 8 heads -> 2 groups), more chunks than heads, d_qk=192,
+# and query-head sub-ranges sharing one copied K/V head
 CASES = [
     (1, 8, 8, 512, 128, "lean", 0),
     (1, 8, 8, 512, 128, "lean", 3),
@@ -24,6 +25,10 @@ CASES = [
     (2, 4, 4, 256, 192, "exact", 1),
     (2, 4, 1, 640, 128, "lean_nobs", 4),
     (1, 2, 2, 256, 128, "exact_nobs", 32),
+    # fewer K/V heads than chunks: query heads split, K and V copied once
+    (1, 8, 1, 384, 128, "lean", 8),
+    (1, 16, 2, 256, 128, "exact", 8),
+    (2, 6, 1, 256, 192, "lean", 5),
 ]
 
 
