@@ -313,3 +313,12 @@ def test_host_plan_shapes_used_by_the_bench(lib):
 def test_host_plan_errors(lib, args, want):
     assert Z.zyfa_fwd_host_plan(*args) == want
     assert Z.load().zyfa_fwd_host_plan(1, 4, 4, 0, None, 3) == Z.ZYFA_ERR_NULL
+
+
+def test_host_binding_rejects_device_or_strided_tensors(lib):
+    import torch
+    q = torch.zeros((1, 256, 2, 128), dtype=torch.uint8)
+    with pytest.raises(ValueError):                  # a BHSD view is not contiguous
+        Z.attention_fp8_host(q.transpose(1, 2).contiguous().transpose(1, 2), q, q)
+    with pytest.raises(ValueError):                  # K's sequence length differs
+        Z.attention_fp8_host(q, q[:, :128], q[:, :128])
