@@ -37,8 +37,8 @@ METRIC = "FP8 causal prefill attn TFLOPS (N=32K, d=128 and MLA 192/128), % of FP
 UNIT = "TFLOP/s"
 FP8_OVER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor ratio (4.5 / 2.25 PF)
 KERNEL_SOURCES = ["fp8_causal_flashattention_gb300/csrc/fwd.cuh",
-                  "fp8_causal_flashattention_gb300/csrc/fwd2.cuh",
                   "fp8_causal_flashattention_gb300/csrc/fwd3.cuh",
+                  "fp8_causal_flashattention_gb300/csrc/fwd4.cuh",
                   "fp8_causal_flashattention_gb300/csrc/ptx.cuh",
                   "fp8_causal_flashattention_gb300/csrc/zyfa_api.cu"]
 

@@ -8,7 +8,7 @@ import subprocess
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libzyfa.so")
 SOURCES = [os.path.join(_HERE, "csrc", f) for f in ("zyfa_api.cu", "quant.cu", "merge.cu", "host.cu")]
-DEPENDS = SOURCES + [os.path.join(_HERE, "csrc", f) for f in ("fwd.cuh", "fwd2.cuh", "fwd3.cuh", "ptx.cuh")] + [
+DEPENDS = SOURCES + [os.path.join(_HERE, "csrc", f) for f in ("fwd.cuh", "fwd3.cuh", "fwd4.cuh", "ptx.cuh")] + [
     os.path.join(os.path.dirname(_HERE), "include", "zyfa.h")]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 

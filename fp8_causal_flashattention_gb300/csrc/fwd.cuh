@@ -149,6 +149,48 @@ __device__ __forceinline__ uint32_t lean_word(float s, float a, float b) {
     return __float_as_uint(fmaf(z, 256.0f, 12582912.0f));
 }
 
+// The rounding step of lean_word on a pair: (z0, z1) * 256 + 1.5 * 2^23 with
+// one packed FMA (each half rounds like the scalar FMA); the codes end up in
+// the low bytes of the returned words.
+__device__ __forceinline__ void lean_word2(float z0, float z1, uint32_t& w0, uint32_t& w1) {
+    asm("{\n\t.reg .b64 Z, K, C;\n\t"
+        "mov.b64 Z, {%2, %3};\n\tmov.b64 K, {%4, %4};\n\tmov.b64 C, {%5, %5};\n\t"
+        "fma.rn.f32x2 Z, Z, K, C;\n\tmov.b64 {%0, %1}, Z;\n\t}"
+        : "=r"(w0), "=r"(w1)
+        : "f"(z0), "f"(z1), "f"(256.0f), "f"(12582912.0f));
+}
+
+// Lean P codes of four scores in one word (key 4w + i in byte i): the
+// saturating FMA of lean_word per score, then the rounding step on two pairs
+// with packed FMAs (k256 = (256, 256), magic = (1.5 * 2^23, 1.5 * 2^23) as
+// packed pairs, built once by the caller) and three byte permutes.
+__device__ __forceinline__ uint32_t lean4(float s0, float s1, float s2, float s3, float a, float b,
+                                          uint64_t k256, uint64_t magic) {
+    uint32_t w;
+    asm("{\n\t.reg .f32 z0, z1, z2, z3;\n\t.reg .b64 p0, p1;\n\t.reg .b32 w0, w1, w2, w3, t0, t1;\n\t"
+        "fma.rn.sat.f32 z0, %1, %5, %6;\n\t"
+        "fma.rn.sat.f32 z1, %2, %5, %6;\n\t"
+        "fma.rn.sat.f32 z2, %3, %5, %6;\n\t"
+        "fma.rn.sat.f32 z3, %4, %5, %6;\n\t"
+        "mov.b64 p0, {z0, z1};\n\t"
+        "mov.b64 p1, {z2, z3};\n\t"
+        "fma.rn.f32x2 p0, p0, %7, %8;\n\t"
+        "fma.rn.f32x2 p1, p1, %7, %8;\n\t"
+        "mov.b64 {w0, w1}, p0;\n\t"
+        "mov.b64 {w2, w3}, p1;\n\t"
+        "prmt.b32 t0, w0, w1, 0x0040;\n\t"
+        "prmt.b32 t1, w2, w3, 0x0040;\n\t"
+        "prmt.b32 %0, t0, t1, 0x5410;\n\t}"
+        : "=r"(w)
+        : "f"(s0), "f"(s1), "f"(s2), "f"(s3), "f"(a), "f"(b), "l"(k256), "l"(magic));
+    return w;
+}
+
+// Two floats packed as the 64-bit operand of a packed FP32 instruction.
+__device__ __forceinline__ uint64_t pack2f(float lo, float hi) {
+    return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+
 // (a, b) *= f on the bit patterns of two FP32 values, one packed multiply.
 __device__ __forceinline__ void mul2s(uint32_t& a, uint32_t& b, float f) {
     asm("{\n\t.reg .b64 Z, K;\n\t"

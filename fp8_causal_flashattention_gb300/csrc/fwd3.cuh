@@ -1,13 +1,15 @@
 // fwd3.cuh -- FP8 attention forward with two query tiles per CTA and two
 // softmax warpgroups per tile (sm_103a).
 //
-// Same method as fwd.cuh and fwd2.cuh ("ZYFA: Speed and Accuracy of FP8
-// FlashAttention on AMD CDNA4": running maximum with lazy rescaling, Sec.
-// II-B and IV-A; Lean P and exact P, Sec. IV-B1; per-64-key block scaling,
-// Sec. IV-B2; division by the sum of the rounded probabilities, Sec. IV-B3),
-// with the loads, MMAs, barriers and TMEM map of fwd2.cuh.  What differs is
-// the softmax: each tile has one warpgroup per 64-key score half.  Half h of
-// block j is read by warpgroup h, which releases the score buffer at once
+// Same method as fwd.cuh ("ZYFA: Speed and Accuracy of FP8 FlashAttention
+// on AMD CDNA4": running maximum with lazy rescaling, Sec. II-B and IV-A;
+// Lean P and exact P, Sec. IV-B1; per-64-key block scaling, Sec. IV-B2;
+// division by the sum of the rounded probabilities, Sec. IV-B3).  One CTA
+// owns query tiles 2p and 2p + 1, both fed by one K/V ring; TMEM per tile
+// holds one 64-key score half, O, L and the scale factors, and P is staged
+// in shared memory for an SS block-scaled PV.  The softmax: each tile has
+// one warpgroup per 64-key score half.  Half h of block j is read by
+// warpgroup h, which releases the score buffer at once
 // (so the tile's next QK half starts), and the two warpgroups exchange their
 // half maxima through two TMEM columns; both then apply the lazy rule to the
 // same numbers (so both hold the same running maximum), each computes the
@@ -19,14 +21,14 @@
 // Warps 0-15 are softmax (warpgroup w: tile w >> 1, half w & 1); warps 16 /
 // 17 issue QK for tiles A / B, 18 / 19 PV (18 also issues the TMA loads).
 // 640 threads with 96 registers each (one CTA per SM): a softmax thread holds
-// 64 scores instead of fwd2.cuh's 128.
+// 64 scores.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cstdint>
 #include <type_traits>
 
-#include "fwd2.cuh"
+#include "fwd.cuh"
 
 namespace zyfa {
 

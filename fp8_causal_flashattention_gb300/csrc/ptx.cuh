@@ -14,7 +14,9 @@ constexpr uint32_t kIdleWaitNs = 500;   // longest sleep of a polling issuer wit
 
 // Device status word read back by zyfa_last_device_status().
 //   0 = ok; otherwise (site << 8) | 1 for a wait that ran out.
-// (The library is one translation unit, so the definition lives here.)
+// Only zyfa_api.cu includes this header and the kernels that use it (the
+// other translation units, quant.cu, merge.cu and host.cu, do not), so the
+// definition lives here and the library holds exactly one copy.
 __device__ int g_device_status = 0;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -76,12 +78,37 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The part of mbar_wait after a first try found the phase incomplete: one
+// out-of-line copy (the polling loop, the timer and the abort bookkeeping
+// are cold code that every wait would otherwise inline).
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
+                                            volatile int* abort_flag, int site) {
+    unsigned long long t0 = globaltimer();
+    for (;;) {
+        if (mbar_try(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kWaitBudgetNs) {
+            *abort_flag = 1;
+            atomicCAS(&g_device_status, 0, (site << 8) | 1);
+            return false;
+        }
+    }
+}
+
 // Waits for the phase of parity `parity` to complete.  Returns false (and
 // leaves the barrier alone) when the CTA has already aborted or when the
 // wait budget runs out; in the latter case it raises the abort flag and
 // records `site` in the device status word.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile int* abort_flag, int site) {
+    if (mbar_try(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort_flag, site);
+}
+
+// mbar_wait with the slow path inline, for code that holds so many live
+// registers that a call would not fit.
+__device__ __forceinline__ bool mbar_wait_inl(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag, int site) {
     if (mbar_try(bar, parity)) return true;
     unsigned long long t0 = globaltimer();
     for (;;) {

@@ -9,8 +9,8 @@
 
 #include "../../include/zyfa.h"
 #include "fwd.cuh"
-#include "fwd2.cuh"
 #include "fwd3.cuh"
+#include "fwd4.cuh"
 
 namespace zyfa {
 namespace {
@@ -111,30 +111,6 @@ int check_common(const void* q, const void* k, const void* v, void* out, int B, 
     return 1;   // proceed
 }
 
-// Two query tiles per CTA, one softmax warpgroup per tile (fwd2.cuh), FP8
-// only.  Not dispatched (never instantiated): fwd3.cuh replaced it for Lean P
-// at d_qk = 128.
-template <int DQK>
-int launch2(const void* q, const void* k, const void* v, const FwdArgs& a, const Layout4& L,
-            cudaStream_t stream) {
-    using C = Fwd2Cfg<DQK>;
-    CUtensorMap tq, tk, tv;
-    const CUtensorMapSwizzle swz =
-        C::CB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    if (!make_map(&tq, q, false, DQK, a.Hq, a.N, a.B, L.q, C::CB, swz)) return ZYFA_ERR_CUDA;
-    if (!make_map(&tk, k, false, DQK, a.Hkv, a.N, a.B, L.k, C::CB, swz)) return ZYFA_ERR_CUDA;
-    if (!make_map(&tv, v, false, C::DV, a.Hkv, a.N, a.B, L.v, 128, CU_TENSOR_MAP_SWIZZLE_128B))
-        return ZYFA_ERR_CUDA;
-    auto kern = zyfa_fwd2_kernel<DQK>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
-        cudaSuccess)
-        return ZYFA_ERR_CUDA;
-    const int T = a.N / C::BM;
-    const unsigned grid = static_cast<unsigned>(a.B) * a.Hq * ((T + 1) / 2);
-    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, a);
-    return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
-}
-
 // Two query tiles per CTA, two softmax warpgroups per tile (fwd3.cuh).
 template <int DQK>
 int launch3(const void* q, const void* k, const void* v, const FwdArgs& a, const Layout4& L,
@@ -153,6 +129,34 @@ int launch3(const void* q, const void* k, const void* v, const FwdArgs& a, const
         return ZYFA_ERR_CUDA;
     const int T = a.N / C::BM;
     const unsigned grid = static_cast<unsigned>(a.B) * a.Hq * ((T + 1) / 2);
+    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, a);
+    return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
+}
+
+// Persistent grid over causal tile pairs, one query tile in flight per CTA
+// (fwd4.cuh): as many CTAs as SMs, or work items if fewer.
+template <int DQK>
+int launch4(const void* q, const void* k, const void* v, const FwdArgs& a, const Layout4& L,
+            cudaStream_t stream) {
+    using C = Fwd4Cfg<DQK>;
+    CUtensorMap tq, tk, tv;
+    const CUtensorMapSwizzle swz =
+        C::CB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!make_map(&tq, q, false, DQK, a.Hq, a.N, a.B, L.q, C::CB, swz)) return ZYFA_ERR_CUDA;
+    if (!make_map(&tk, k, false, DQK, a.Hkv, a.N, a.B, L.k, C::CB, swz)) return ZYFA_ERR_CUDA;
+    if (!make_map(&tv, v, false, C::DV, a.Hkv, a.N, a.B, L.v, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+        return ZYFA_ERR_CUDA;
+    auto kern = a.p_mode == ZYFA_P_LEAN ? zyfa_fwd4_kernel<DQK, 1> : zyfa_fwd4_kernel<DQK, 0>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
+        cudaSuccess)
+        return ZYFA_ERR_CUDA;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return ZYFA_ERR_CUDA;
+    const int T = a.N / C::BM;
+    const long long items = static_cast<long long>(a.B) * a.Hq * ((T + 1) / 2);
+    const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
     kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, a);
     return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
 }
@@ -176,6 +180,16 @@ int launch(const void* q, const void* k, const void* v, const FwdArgs& a, const 
     const unsigned grid = static_cast<unsigned>(a.B) * a.Hq * (a.N / C::BM);
     kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, a);
     return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
+}
+
+// The FP8 forward's kernel per mode, by measurement on GB300: Lean P at
+// d_qk = 128 runs the two-tile kernel (fwd3.cuh), exact P and d_qk = 192 the
+// persistent one-tile kernel over causal pairs (fwd4.cuh).
+int dispatch_fp8(const void* q, const void* k, const void* v, const FwdArgs& a, const Layout4& L,
+                 cudaStream_t s, int d_qk) {
+    if (d_qk == 192) return launch4<192>(q, k, v, a, L, s);
+    if (a.p_mode == ZYFA_P_LEAN) return launch3<128>(q, k, v, a, L, s);
+    return launch4<128>(q, k, v, a, L, s);
 }
 
 }  // namespace
@@ -215,12 +229,7 @@ extern "C" int zyfa_fwd_strided(const void* q, const void* k, const void* v,
     FwdArgs a{out, lse, descale_q, descale_k, descale_v, B, Hq, Hkv, N, p_mode, block_scale,
               causal, 1.0f / sqrtf(static_cast<float>(d_qk)), L.o.b, L.o.n, L.o.h};
     auto s = static_cast<cudaStream_t>(stream);
-    // Lean P at d_qk = 128: two query tiles per CTA with two softmax
-    // warpgroups per tile (fwd3.cuh).  Exact P is bound by the ex2 unit, and
-    // at d_qk = 192 two Q tiles and double-buffered P leave shared memory for
-    // two K/V stages only; there one tile per CTA (fwd.cuh) measures faster.
-    if (p_mode == ZYFA_P_LEAN && d_qk == 128) return launch3<128>(q, k, v, a, L, s);
-    return d_qk == 128 ? launch<true, 128>(q, k, v, a, L, s) : launch<true, 192>(q, k, v, a, L, s);
+    return dispatch_fp8(q, k, v, a, L, s, d_qk);
 }
 
 extern "C" int zyfa_fwd_ex(const void* q, const void* k, const void* v, const float* descale_q,
@@ -297,8 +306,7 @@ extern "C" int zyfa_fwd_partial(const void* q, const void* k, const void* v,
               key_begin / 128, key_end / 128};
     auto s = static_cast<cudaStream_t>(stream);
     // the kernels of zyfa_fwd_strided, which all read the key range
-    if (p_mode == ZYFA_P_LEAN && d_qk == 128) return launch3<128>(q, k, v, a, L, s);
-    return d_qk == 128 ? launch<true, 128>(q, k, v, a, L, s) : launch<true, 192>(q, k, v, a, L, s);
+    return dispatch_fp8(q, k, v, a, L, s, d_qk);
 }
 
 extern "C" int zyfa_fwd_bf16_partial(const void* q, const void* k, const void* v, void* out,
