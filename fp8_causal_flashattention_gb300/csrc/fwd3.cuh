@@ -18,6 +18,8 @@
 // L, and publishes P_j together with the half-0 warpgroup (p_full counts
 // both).  Each warpgroup writes 64 of the 128 output columns.
 //
+// Lean P only (the launcher sends exact P to fwd4.cuh).
+//
 // Warps 0-15 are softmax (warpgroup w: tile w >> 1, half w & 1); warps 16 /
 // 17 issue QK for tiles A / B, 18 / 19 PV (18 also issues the TMA loads).
 // 640 threads with 96 registers each (one CTA per SM): a softmax thread holds
@@ -364,32 +366,14 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         bool ok = true;
 
         // e4m3 codes of 16 scores relative to maximum m with block exponent o
+        const uint64_t k256 = pack2f(256.0f, 256.0f);
+        const uint64_t magic = pack2f(12582912.0f, 12582912.0f);
         auto codes16 = [&](const float* q, float m, int o) -> uint4 {
             uint32_t pw[4];
-            if (args.p_mode == 1) {
-                const float bb = (8.0f * (kSigma + 7.0f + (float)o - m) - kBeta) * (1.0f / 256.0f);
-                #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    // saturating FMA per score, then the rounding FMA on pairs
-                    uint32_t q0, q1, q2, q3;
-                    lean_word2(fma_sat(q[4 * w + 0], a_lean, bb), fma_sat(q[4 * w + 1], a_lean, bb),
-                               q0, q1);
-                    lean_word2(fma_sat(q[4 * w + 2], a_lean, bb), fma_sat(q[4 * w + 3], a_lean, bb),
-                               q2, q3);
-                    pw[w] = __byte_perm(__byte_perm(q0, q1, 0x0040), __byte_perm(q2, q3, 0x0040),
-                                        0x5410);
-                }
-            } else {
-                const float ee = kSigma + (float)o - m;
-                #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float p0 = ex2(fmaf(q[4 * w + 0], A1, ee));
-                    const float p1 = ex2(fmaf(q[4 * w + 1], A1, ee));
-                    const float p2 = ex2(fmaf(q[4 * w + 2], A1, ee));
-                    const float p3 = ex2(fmaf(q[4 * w + 3], A1, ee));
-                    pw[w] = cvt_e4m3x2(p0, p1) | (cvt_e4m3x2(p2, p3) << 16);
-                }
-            }
+            const float bb = (8.0f * (kSigma + 7.0f + (float)o - m) - kBeta) * (1.0f / 256.0f);
+            #pragma unroll
+            for (int w = 0; w < 4; ++w)
+                pw[w] = lean4(q[4 * w + 0], q[4 * w + 1], q[4 * w + 2], q[4 * w + 3], a_lean, bb, k256, magic);
             return make_uint4(pw[0], pw[1], pw[2], pw[3]);
         };
         // whole binades between the 64-key block maximum and the row maximum

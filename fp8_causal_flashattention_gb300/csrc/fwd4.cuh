@@ -120,8 +120,8 @@ struct Fwd4Cfg {
 struct TileIter {
     int b, g, p, hh;       // current item
     int half;              // 0: the pair's long tile T-1-p, 1: its short tile p
-    int db, dg, dp, dh;    // G in the same digits
-    int grp, npair;        // query heads per KV head, pairs per head
+    uint32_t gdig;         // G's digits (hh, p, g, b) in bytes 0-3 (G <= 255 CTAs)
+    uint32_t radix;        // query heads per KV head (low 16 bits), pairs per head
     int qt, h;             // current tile: query tile and head
     int nb;                // key blocks of the range it sees (0: output zeros)
     bool valid;            // false past the last item
@@ -129,7 +129,7 @@ struct TileIter {
 
 __device__ __forceinline__ void tiles_set(TileIter& it, const FwdArgs& a, int T) {
     it.qt = it.half ? it.p : T - 1 - it.p;
-    it.h = it.g * it.grp + it.hh;
+    it.h = it.g * static_cast<int>(it.radix & 0xFFFFu) + it.hh;
     const int lim = a.causal ? it.qt + 1 : T;
     const int end = lim < a.kb1 ? lim : a.kb1;
     it.nb = end > a.kb0 ? end - a.kb0 : 0;
@@ -137,11 +137,12 @@ __device__ __forceinline__ void tiles_set(TileIter& it, const FwdArgs& a, int T)
 
 __device__ __forceinline__ void tiles_begin(TileIter& it, const FwdArgs& a, int T) {
     const unsigned npair = (T + 1) / 2, grp = a.Hq / a.Hkv, hkv = a.Hkv;
-    it.grp = grp;
-    it.npair = npair;
+    it.radix = grp | (npair << 16);
     unsigned x = blockIdx.x, y = gridDim.x;
     it.hh = x % grp;  x /= grp;  it.p = x % npair;  x /= npair;  it.g = x % hkv;  it.b = x / hkv;
-    it.dh = y % grp;  y /= grp;  it.dp = y % npair; y /= npair;  it.dg = y % hkv;  it.db = y / hkv;
+    const unsigned dh = y % grp;  y /= grp;
+    const unsigned dp = y % npair; y /= npair;
+    it.gdig = dh | (dp << 8) | ((y % hkv) << 16) | ((y / hkv) << 24);
     it.half = 0;
     it.valid = it.b < a.B;
     if (it.valid) tiles_set(it, a, T);
@@ -151,13 +152,14 @@ __device__ __forceinline__ void tiles_next(TileIter& it, const FwdArgs& a, int T
     if (it.half == 0 && it.p != T - 1 - it.p) {
         it.half = 1;
     } else {
+        const int grp = static_cast<int>(it.radix & 0xFFFFu), npair = static_cast<int>(it.radix >> 16);
         it.half = 0;
-        it.hh += it.dh;
-        it.p += it.dp;
-        it.g += it.dg;
-        it.b += it.db;
-        if (it.hh >= it.grp) { it.hh -= it.grp; ++it.p; }
-        if (it.p >= it.npair) { it.p -= it.npair; ++it.g; }
+        it.hh += static_cast<int>(it.gdig & 0xFFu);
+        it.p += static_cast<int>((it.gdig >> 8) & 0xFFu);
+        it.g += static_cast<int>((it.gdig >> 16) & 0xFFu);
+        it.b += static_cast<int>(it.gdig >> 24);
+        if (it.hh >= grp) { it.hh -= grp; ++it.p; }
+        if (it.p >= npair) { it.p -= npair; ++it.g; }
         if (it.g >= a.Hkv) { it.g -= a.Hkv; ++it.b; }
         it.valid = it.b < a.B;
     }

@@ -111,7 +111,7 @@ int check_common(const void* q, const void* k, const void* v, void* out, int B, 
     return 1;   // proceed
 }
 
-// Two query tiles per CTA, two softmax warpgroups per tile (fwd3.cuh).
+// Two query tiles per CTA, two softmax warpgroups per tile (fwd3.cuh), Lean P.
 template <int DQK>
 int launch3(const void* q, const void* k, const void* v, const FwdArgs& a, const Layout4& L,
             cudaStream_t stream) {
@@ -156,7 +156,9 @@ int launch4(const void* q, const void* k, const void* v, const FwdArgs& a, const
         return ZYFA_ERR_CUDA;
     const int T = a.N / C::BM;
     const long long items = static_cast<long long>(a.B) * a.Hq * ((T + 1) / 2);
-    const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
+    // the kernel keeps the grid's mixed-radix digits in bytes (grid <= 255)
+    const long long cap = sms < 255 ? sms : 255;
+    const unsigned grid = static_cast<unsigned>(items < cap ? items : cap);
     kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, a);
     return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
 }
