@@ -351,19 +351,36 @@ def run_ours(args, wl: S.Workload):
 
 def extras(args, P, fp8_peak, bf16_peak):
     """The other measured points: BF16 and exact P at d=128, and the MLA shape
-    (exact P, the paper's default there, and Lean P), device-timed alike."""
+    (exact P, the paper's default there, and Lean P), device-timed alike, each
+    over as many launches as the headline (at least 20).  The MLA shape is
+    half of the metric, so its lines carry a roofline block and the clocks of
+    their timed region too."""
     import torch
     res = {}
     stream = torch.cuda.current_stream()
-    steps = max(3, min(args.steps // 4, 50))
+    steps = max(20, args.steps)
     for name, mode in (("d128", "bf16"), ("d128", "exact"), ("mla", "exact"), ("mla", "lean")):
         wl = S.WORKLOADS[name]
         inp = S.make_inputs(wl, fp8=mode != "bf16", bf16=mode == "bf16")
         dev = P.to_device(inp, mode != "bf16")
-        ms = time_launches(lambda: P.gpu_run(inp, mode, dev), steps, 3, stream)
+        run = lambda: P.gpu_run(inp, mode, dev)
+        for _ in range(3):
+            run()
+        clk = ClockSampler(None)
+        clk.start()
+        time.sleep(0.2)
+        ms = time_launches(run, steps, 0, stream)
+        clocks = clk.stop()
         tf = wl.causal_flops / (ms * 1e-3) / 1e12
         peak = bf16_peak if mode == "bf16" else fp8_peak
-        res[f"{name}_{mode}"] = {"tflops": tf, "ms": ms, "frac_of_peak": tf / peak}
+        entry = {"tflops": tf, "ms": ms, "frac_of_peak": tf / peak, "launches": steps,
+                 "clocks": clocks}
+        if name == "mla":
+            entry["roofline"] = {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                                 "frac": tf / peak,
+                                 "traffic": stored_traffic(f"{name}_{mode}"),
+                                 "algorithmic": "F = B*Hq*N^2*(d_qk+d_v) causal FLOPs per launch"}
+        res[f"{name}_{mode}"] = entry
         del dev, inp
         torch.cuda.empty_cache()
     # BF16 QK^T with FP8 PV (the variant the paper's conclusion recommends)

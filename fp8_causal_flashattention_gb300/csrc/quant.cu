@@ -18,6 +18,7 @@
 // Everything is FP32, as the paper prescribes for the rotation.  Sums and
 // maxima are deterministic: the mean is reduced in a fixed order (per-chunk
 // partial sums, then a fixed-order finalise), the maximum is order-free.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cfloat>
@@ -690,9 +691,11 @@ extern "C" int zyfa_quantize(const void* x, const float* signs, int smooth, floa
 // allocator that the library must not draw from.
 //
 // The array lives at file scope, one copy per device, 16 MiB.  Its address
-// is looked up once per device with cudaGetSymbolAddress; that first call on
+// is looked up with cudaGetSymbolAddress once per device and context (again
+// after a reset gives the device a new primary context); the first lookup on
 // a device may load the module, so it must not happen inside a stream
-// capture.  Only the per-call maximum word must start at zero; it is zeroed
+// capture.  `stream` must belong to the current device, whose copy of the
+// array the call uses.  Only the per-call maximum word must start at zero; it is zeroed
 // on the stream (cudaMemsetAsync) before the maximum pass of every call, and
 // everything else in the array is written before it is read.  All calls on a
 // device share the array: two calls whose work overlaps in time (different
@@ -705,17 +708,49 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch on the current device (cached).
+// The context current on this thread (the driver's cuCtxGetCurrent, found
+// through the runtime so that the library needs no link to the driver).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CUcontext current_context() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    CUcontext c = nullptr;
+    if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
+
+// Device address of g_noalloc_scratch on the current device: looked up once
+// per device and cached together with the context it was found in, and
+// looked up again when the device's context has changed (a device reset
+// destroys the primary context, and the module's memory with it).
 char* noalloc_scratch() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    void* p = nullptr;
+    CUcontext ctx = current_context();
+    if (!ctx) {
+        // no context current on this thread yet: the lookup makes the
+        // device's primary context current
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+        ctx = current_context();
+        if (!ctx) return nullptr;
+    }
     static std::mutex mu;
     static void* addr[kMaxDevices] = {};
+    static CUcontext owner[kMaxDevices] = {};
     std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    if (!addr[dev] || owner[dev] != ctx) {
+        if (!p && cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
         addr[dev] = p;
+        owner[dev] = ctx;
     }
     return static_cast<char*>(addr[dev]);
 }
@@ -754,6 +789,13 @@ extern "C" int zyfa_quantize_noalloc(const void* x, const float* signs, int smoo
     const size_t bytes = amax_bytes + (partial_floats + mean_floats) * sizeof(float);
     const bool need_scratch = dynamic || sm;
     if (need_scratch && bytes > kNoAllocScratchBytes) return ZYFA_ERR_SCRATCH;
+    if (need_scratch) {
+        // the array used is the current device's: the stream must run there
+        int cur = 0, sdev = 0;
+        if (cudaGetDevice(&cur) != cudaSuccess || cudaStreamGetDevice(s, &sdev) != cudaSuccess)
+            return ZYFA_ERR_CUDA;
+        if (sdev != cur) return ZYFA_ERR_UNSUPPORTED;
+    }
     char* sp = need_scratch ? noalloc_scratch() : nullptr;
     if (need_scratch && !sp) return ZYFA_ERR_CUDA;
     sa.partial = sm ? reinterpret_cast<float*>(sp + amax_bytes) : nullptr;

@@ -177,7 +177,13 @@ int zyfa_quantize(const void* x, const float* signs, int smooth, float static_de
  *     for B = 1, H = 32, D = 128, N = 32768.
  *   - The first call on each device looks the array up with
  *     cudaGetSymbolAddress, which may load the module: make it outside any
- *     stream capture.
+ *     stream capture.  The address is kept per device together with the
+ *     context it was found in; a call that finds another context current
+ *     (after a device reset) looks it up again, which is then such a first
+ *     call.
+ *   - The array used is the current device's: `stream` must belong to the
+ *     current device (ZYFA_ERR_UNSUPPORTED otherwise, checked before
+ *     anything is launched, when the call needs scratch).
  *   - The maximum word is zeroed on `stream` by every call that uses it;
  *     the rest of the scratch is written before it is read.
  *   - All calls on one device share the array: calls whose work overlaps in

@@ -122,6 +122,19 @@ def test_quantize_argument_errors(lib, args, want):
     assert rc == want
 
 
+def test_quantize_noalloc_rejects_oversize_before_launch(lib):
+    """zyfa_quantize_noalloc: a smoothing call whose partial sums exceed the
+    library's 16 MiB buffer returns ZYFA_ERR_SCRATCH before anything is
+    launched (the pointers are never dereferenced, no GPU is needed)."""
+    B, N, H, D = 4096, 4, 128, 192            # 4 x 4096 x 128 x 192 bytes of partial sums
+    rc = Z.zyfa_quantize_noalloc(FAKE, None, 1, 0.0, FAKE, FAKE, FAKE, B, N, H, D, 0)
+    assert rc == Z.ZYFA_ERR_SCRATCH
+    assert "scratch" in Z.zyfa_status_string(rc)
+    # without smoothing and with a static scale no scratch is needed: the
+    # NULL x is reported first
+    assert Z.zyfa_quantize_noalloc(None, None, 0, 1.0, FAKE, FAKE, None, B, N, H, D, 0) == Z.ZYFA_ERR_NULL
+
+
 def _bshd(B, N, H, d):
     return [N * H * d, H * d, d]
 
