@@ -389,13 +389,16 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 break;
             tc_fence_after();
             float s[64];
+            float hm;                                           // maximum of the half
             {
                 uint32_t r[64];
-                tmem_ld32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                float m0, m1;
+                tmem_ld32_max(t_s, *reinterpret_cast<uint32_t(*)[32]>(&r[0]), m0);
+                tmem_ld32_max(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]), m1);
                 tmem_wait_ld();
                 #pragma unroll
                 for (int k = 0; k < 64; ++k) s[k] = __uint_as_float(r[k]);
+                hm = fmaxf(m0, m1);
             }
             tc_fence_before();
             mbar_arrive(BAR(B_SX + t));
@@ -403,9 +406,7 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 #pragma unroll
                 for (int k = 0; k < 64; ++k)
                     if (64 * hf + k > row) s[k] = -INFINITY;
-            }
-            float hm;
-            {
+                // the maximum again, over the unmasked keys
                 float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
                 #pragma unroll
                 for (int k = 4; k + 8 <= 64; k += 8) {

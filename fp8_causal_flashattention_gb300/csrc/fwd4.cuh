@@ -338,12 +338,22 @@ zyfa_fwd4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
             };
             // pass 1: the maxima of the two 64-key halves
+            // (off the diagonal the loads return them; on it, after the mask)
             float hs0 = -INFINITY, hs1 = -INFINITY;
             #pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
                 float h[64];
-                load_half(hf, h);
-                const float mh = max64(h);
+                float mh;
+                if (!diag) {
+                    float m0, m1;
+                    tmem_ld32_max(t_s + 64 * hf, *reinterpret_cast<uint32_t(*)[32]>(&h[0]), m0);
+                    tmem_ld32_max(t_s + 64 * hf + 32, *reinterpret_cast<uint32_t(*)[32]>(&h[32]), m1);
+                    tmem_wait_ld();
+                    mh = fmaxf(m0, m1);
+                } else {
+                    load_half(hf, h);
+                    mh = max64(h);
+                }
                 if (hf == 0) hs0 = mh; else hs1 = mh;
             }
             // running max after block g - 1 from the other warpgroup (its slot
