@@ -112,11 +112,6 @@ struct FwdCfg {
     static constexpr int THREADS = NSM + 64;
 };
 
-__device__ __forceinline__ float fma_sat(float a, float b, float c) {
-    float d;
-    asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -127,43 +122,20 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
 }
-// e4m3 codes of (lo, hi) in bytes 0 and 1, round to nearest even, saturating.
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
 __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
 
-// Lean P of one score: the low byte of the returned word is the e4m3 code
-// clamp(rne(a*s + b'), 0, 255) with a = 8 A/256, b' = (8(sigma+7+o-m) - beta)/256:
-// the saturating FMA clamps y/256 to [0, 1] (a NaN score gives 0) and adding
-// 1.5 * 2^23 after scaling by 256 rounds y to the nearest integer in the low
-// mantissa bits.
-__device__ __forceinline__ uint32_t lean_word(float s, float a, float b) {
-    float z = fma_sat(s, a, b);
-    return __float_as_uint(fmaf(z, 256.0f, 12582912.0f));
-}
-
-// The rounding step of lean_word on a pair: (z0, z1) * 256 + 1.5 * 2^23 with
-// one packed FMA (each half rounds like the scalar FMA); the codes end up in
-// the low bytes of the returned words.
-__device__ __forceinline__ void lean_word2(float z0, float z1, uint32_t& w0, uint32_t& w1) {
-    asm("{\n\t.reg .b64 Z, K, C;\n\t"
-        "mov.b64 Z, {%2, %3};\n\tmov.b64 K, {%4, %4};\n\tmov.b64 C, {%5, %5};\n\t"
-        "fma.rn.f32x2 Z, Z, K, C;\n\tmov.b64 {%0, %1}, Z;\n\t}"
-        : "=r"(w0), "=r"(w1)
-        : "f"(z0), "f"(z1), "f"(256.0f), "f"(12582912.0f));
-}
-
-// Lean P codes of four scores in one word (key 4w + i in byte i): the
-// saturating FMA of lean_word per score, then the rounding step on two pairs
-// with packed FMAs (k256 = (256, 256), magic = (1.5 * 2^23, 1.5 * 2^23) as
-// packed pairs, built once by the caller) and three byte permutes.
+// Lean P codes of four scores in one word (key 4w + i in byte i).  The code
+// of score s is clamp(rne(y), 0, 255) with y = 8 A s + 8(sigma+7+o-m) - beta,
+// passed as a = 8 A/256 and b = (8(sigma+7+o-m) - beta)/256: the saturating
+// FMA per score clamps y/256 to [0, 1] (a NaN score gives 0); scaling by 256
+// and adding 1.5 * 2^23, one packed FMA per pair (k256 = (256, 256), magic =
+// (1.5 * 2^23, 1.5 * 2^23), built once by the caller; each half rounds like
+// the scalar FMA), rounds y to the nearest integer in the low mantissa bits;
+// three byte permutes gather the four low bytes.
 __device__ __forceinline__ uint32_t lean4(float s0, float s1, float s2, float s3, float a, float b,
                                           uint64_t k256, uint64_t magic) {
     uint32_t w;
@@ -183,6 +155,32 @@ __device__ __forceinline__ uint32_t lean4(float s0, float s1, float s2, float s3
         "prmt.b32 %0, t0, t1, 0x5410;\n\t}"
         : "=r"(w)
         : "f"(s0), "f"(s1), "f"(s2), "f"(s3), "f"(a), "f"(b), "l"(k256), "l"(magic));
+    return w;
+}
+
+// Exact P codes of four scores in one word (key 4w + i in byte i): the
+// exponents x = A s + e for two pairs with packed FMAs (a2 = (A, A), e2 =
+// (e, e)), ex2.approx per score and two e4m3x2 conversions.  Each half of a
+// packed FMA rounds like the scalar FMA, so the codes equal those of
+// ex2(fmaf(s, A, e)).
+__device__ __forceinline__ uint32_t exact4(float s0, float s1, float s2, float s3, uint64_t a2, uint64_t e2) {
+    uint32_t w;
+    asm("{\n\t.reg .b64 p0, p1;\n\t.reg .f32 x0, x1, x2, x3;\n\t.reg .b16 h0, h1;\n\t"
+        "mov.b64 p0, {%1, %2};\n\t"
+        "mov.b64 p1, {%3, %4};\n\t"
+        "fma.rn.f32x2 p0, p0, %5, %6;\n\t"
+        "fma.rn.f32x2 p1, p1, %5, %6;\n\t"
+        "mov.b64 {x0, x1}, p0;\n\t"
+        "mov.b64 {x2, x3}, p1;\n\t"
+        "ex2.approx.ftz.f32 x0, x0;\n\t"
+        "ex2.approx.ftz.f32 x1, x1;\n\t"
+        "ex2.approx.ftz.f32 x2, x2;\n\t"
+        "ex2.approx.ftz.f32 x3, x3;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 h0, x1, x0;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 h1, x3, x2;\n\t"
+        "mov.b32 %0, {h0, h1};\n\t}"
+        : "=r"(w)
+        : "f"(s0), "f"(s1), "f"(s2), "f"(s3), "l"(a2), "l"(e2));
     return w;
 }
 
@@ -554,25 +552,18 @@ zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     uint32_t pw[16];
                     if (args.p_mode == 1) {
                         const float bb = (8.0f * (kSigma + 7.0f + (float)o[sb] - m_i) - kBeta) * (1.0f / 256.0f);
+                        const uint64_t k256 = pack2f(256.0f, 256.0f);
+                        const uint64_t magic = pack2f(12582912.0f, 12582912.0f);
                         #pragma unroll
-                        for (int w = 0; w < 16; ++w) {
-                            const uint32_t q0 = lean_word(q[4 * w + 0], a_lean, bb);
-                            const uint32_t q1 = lean_word(q[4 * w + 1], a_lean, bb);
-                            const uint32_t q2 = lean_word(q[4 * w + 2], a_lean, bb);
-                            const uint32_t q3 = lean_word(q[4 * w + 3], a_lean, bb);
-                            pw[w] = __byte_perm(__byte_perm(q0, q1, 0x0040),
-                                                __byte_perm(q2, q3, 0x0040), 0x5410);
-                        }
+                        for (int w = 0; w < 16; ++w)
+                            pw[w] = lean4(q[4 * w + 0], q[4 * w + 1], q[4 * w + 2], q[4 * w + 3], a_lean, bb, k256,
+                                          magic);
                     } else {
                         const float ee = kSigma + (float)o[sb] - m_i;
+                        const uint64_t a12 = pack2f(A1, A1), e2 = pack2f(ee, ee);
                         #pragma unroll
-                        for (int w = 0; w < 16; ++w) {
-                            const float p0 = ex2(fmaf(q[4 * w + 0], A1, ee));
-                            const float p1 = ex2(fmaf(q[4 * w + 1], A1, ee));
-                            const float p2 = ex2(fmaf(q[4 * w + 2], A1, ee));
-                            const float p3 = ex2(fmaf(q[4 * w + 3], A1, ee));
-                            pw[w] = cvt_e4m3x2(p0, p1) | (cvt_e4m3x2(p2, p3) << 16);
-                        }
+                        for (int w = 0; w < 16; ++w)
+                            pw[w] = exact4(q[4 * w + 0], q[4 * w + 1], q[4 * w + 2], q[4 * w + 3], a12, e2);
                     }
                     tmem_st<16>(t_p + 16 * sb, pw);
                 }

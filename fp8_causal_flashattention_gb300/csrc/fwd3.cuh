@@ -18,7 +18,7 @@
 // L, and publishes P_j together with the half-0 warpgroup (p_full counts
 // both).  Each warpgroup writes 64 of the 128 output columns.
 //
-// Lean P only (the launcher sends exact P to fwd4.cuh).
+// Lean P or exact P (template parameter LEAN).
 //
 // Warps 0-15 are softmax (warpgroup w: tile w >> 1, half w & 1); warps 16 /
 // 17 issue QK for tiles A / B, 18 / 19 PV (18 also issues the TMA loads).
@@ -77,7 +77,8 @@ struct Fwd3Cfg {
     static constexpr uint32_t TMEM_COLS = 512;
 };
 
-template <int DQK>
+// LEAN: 1 Lean P, 0 exact P (one code loop per kernel).
+template <int DQK, int LEAN>
 __global__ void __launch_bounds__(Fwd3Cfg<DQK>::THREADS, 1)
 zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
@@ -368,12 +369,21 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // e4m3 codes of 16 scores relative to maximum m with block exponent o
         const uint64_t k256 = pack2f(256.0f, 256.0f);
         const uint64_t magic = pack2f(12582912.0f, 12582912.0f);
+        const uint64_t a12 = pack2f(A1, A1);
         auto codes16 = [&](const float* q, float m, int o) -> uint4 {
             uint32_t pw[4];
-            const float bb = (8.0f * (kSigma + 7.0f + (float)o - m) - kBeta) * (1.0f / 256.0f);
-            #pragma unroll
-            for (int w = 0; w < 4; ++w)
-                pw[w] = lean4(q[4 * w + 0], q[4 * w + 1], q[4 * w + 2], q[4 * w + 3], a_lean, bb, k256, magic);
+            if constexpr (LEAN == 1) {
+                const float bb = (8.0f * (kSigma + 7.0f + (float)o - m) - kBeta) * (1.0f / 256.0f);
+                #pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    pw[w] = lean4(q[4 * w + 0], q[4 * w + 1], q[4 * w + 2], q[4 * w + 3], a_lean, bb, k256, magic);
+            } else {
+                const float ee = kSigma + (float)o - m;
+                const uint64_t e2 = pack2f(ee, ee);
+                #pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    pw[w] = exact4(q[4 * w + 0], q[4 * w + 1], q[4 * w + 2], q[4 * w + 3], a12, e2);
+            }
             return make_uint4(pw[0], pw[1], pw[2], pw[3]);
         };
         // whole binades between the 64-key block maximum and the row maximum

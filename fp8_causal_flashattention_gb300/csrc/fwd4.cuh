@@ -294,6 +294,7 @@ zyfa_fwd4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         };
         const uint64_t k256 = pack2f(256.0f, 256.0f);
         const uint64_t magic = pack2f(12582912.0f, 12582912.0f);
+        const uint64_t a12 = pack2f(A1, A1);
         // e4m3 codes of 64 scores relative to maximum m with block exponent o
         auto codes64 = [&](const float* q, float m, int o, uint32_t (&pw)[16]) {
             if constexpr (LEAN == 1) {
@@ -303,14 +304,10 @@ zyfa_fwd4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     pw[w] = lean4(q[4 * w + 0], q[4 * w + 1], q[4 * w + 2], q[4 * w + 3], a_lean, bb, k256, magic);
             } else {
                 const float ee = kSigma + (float)o - m;
+                const uint64_t e2 = pack2f(ee, ee);
                 #pragma unroll
-                for (int w = 0; w < 16; ++w) {
-                    const float p0 = ex2(fmaf(q[4 * w + 0], A1, ee));
-                    const float p1 = ex2(fmaf(q[4 * w + 1], A1, ee));
-                    const float p2 = ex2(fmaf(q[4 * w + 2], A1, ee));
-                    const float p3 = ex2(fmaf(q[4 * w + 3], A1, ee));
-                    pw[w] = cvt_e4m3x2(p0, p1) | (cvt_e4m3x2(p2, p3) << 16);
-                }
+                for (int w = 0; w < 16; ++w)
+                    pw[w] = exact4(q[4 * w + 0], q[4 * w + 1], q[4 * w + 2], q[4 * w + 3], a12, e2);
             }
         };
         BlockCur c;

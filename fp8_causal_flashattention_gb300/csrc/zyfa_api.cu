@@ -111,7 +111,7 @@ int check_common(const void* q, const void* k, const void* v, void* out, int B, 
     return 1;   // proceed
 }
 
-// Two query tiles per CTA, two softmax warpgroups per tile (fwd3.cuh), Lean P.
+// Two query tiles per CTA, two softmax warpgroups per tile (fwd3.cuh).
 template <int DQK>
 int launch3(const void* q, const void* k, const void* v, const FwdArgs& a, const Layout4& L,
             cudaStream_t stream) {
@@ -123,7 +123,7 @@ int launch3(const void* q, const void* k, const void* v, const FwdArgs& a, const
     if (!make_map(&tk, k, false, DQK, a.Hkv, a.N, a.B, L.k, C::CB, swz)) return ZYFA_ERR_CUDA;
     if (!make_map(&tv, v, false, C::DV, a.Hkv, a.N, a.B, L.v, 128, CU_TENSOR_MAP_SWIZZLE_128B))
         return ZYFA_ERR_CUDA;
-    auto kern = zyfa_fwd3_kernel<DQK>;
+    auto kern = a.p_mode == ZYFA_P_LEAN ? zyfa_fwd3_kernel<DQK, 1> : zyfa_fwd3_kernel<DQK, 0>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
         cudaSuccess)
         return ZYFA_ERR_CUDA;
@@ -184,17 +184,19 @@ int launch(const void* q, const void* k, const void* v, const FwdArgs& a, const 
     return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
 }
 
-// The FP8 forward's kernel per mode and length, by measurement on GB300:
-// Lean P at d_qk = 128 runs the two-tile kernel (fwd3.cuh) for sequences
-// longer than 2048 (at 4K and beyond it measures 5-15 % faster), everything
-// else the persistent one-tile kernel over causal pairs (fwd4.cuh): exact P,
-// d_qk = 192, and short sequences, where the persistent grid saves the
-// per-CTA setup that dominates short tiles (Lean P at N = 512 / 1K / 2K:
-// +55 / +30 / +9 %).
+// The FP8 forward's kernel per mode and length, by measurement on GB300
+// (outputs bit-identical between the two): at d_qk = 128 the two-tile kernel
+// (fwd3.cuh) for Lean P beyond 2048 keys and exact P beyond 4096 (d128 N =
+// 32K: Lean 1866 against 1609 TFLOP/s, exact 1789 against 1667), the
+// persistent kernel over causal pairs (fwd4.cuh) below that, where the
+// persistent grid saves the per-CTA setup that dominates short tiles (Lean
+// P at N = 512 / 1K / 2K: 718 / 947 / 1125 against 461 / 734 / 1047; exact
+// P at 4K: 1345 against 1298), and at d_qk = 192.
 int dispatch_fp8(const void* q, const void* k, const void* v, const FwdArgs& a, const Layout4& L,
                  cudaStream_t s, int d_qk) {
     if (d_qk == 192) return launch4<192>(q, k, v, a, L, s);
-    if (a.p_mode == ZYFA_P_LEAN && a.N > 2048) return launch3<128>(q, k, v, a, L, s);
+    const int two_tile_above = a.p_mode == ZYFA_P_LEAN ? 2048 : 4096;
+    if (a.N > two_tile_above) return launch3<128>(q, k, v, a, L, s);
     return launch4<128>(q, k, v, a, L, s);
 }
 
