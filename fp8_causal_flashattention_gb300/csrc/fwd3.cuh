@@ -81,7 +81,8 @@ struct Fwd3Cfg {
 template <int DQK, int LEAN>
 __global__ void __launch_bounds__(Fwd3Cfg<DQK>::THREADS, 1)
 zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                 const FwdArgs args) {
     using C = Fwd3Cfg<DQK>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
@@ -518,22 +519,50 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                            static_cast<size_t>(qt) * C::BM + row;
                     args.lse[lse_idx] = logf(l) + (m_run - kSigma) * 0.6931471805599453f;
                 }
-                const long long orow = b * args.o_sb + (static_cast<long long>(qt) * C::BM + row) * args.o_sn +
-                                       h * args.o_sh;
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + orow + 64 * hf);
-                #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(t_row + C::col_o(t) + 64 * hf + c * 32, r);
-                    tmem_wait_ld();
+                auto cvt8 = [&](const uint32_t* r) -> uint4 {
+                    uint4 v4;
+                    v4.x = cvt_bf16x2(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv);
+                    v4.y = cvt_bf16x2(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv);
+                    v4.z = cvt_bf16x2(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv);
+                    v4.w = cvt_bf16x2(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
+                    return v4;
+                };
+                if (args.o_tma) {
+                    // through shared memory and one bulk tensor store per warp
+                    // (32 rows x 64 columns, 128-byte swizzle: 16-byte chunk j of
+                    // row r at position j ^ (r & 7)); the staging is the tile's
+                    // own two P slots, which no MMA reads once its last PV has
+                    // completed (fin)
+                    const uint32_t stg_off = C::OFF_P + 2 * t * C::P_BYTES + ((hf * 4 + (warp & 3)) << 12);
+                    uint8_t* stg = smem + stg_off + lane * 128;
                     #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint4 v4;
-                        v4.x = cvt_bf16x2(__uint_as_float(r[8 * k + 0]) * inv, __uint_as_float(r[8 * k + 1]) * inv);
-                        v4.y = cvt_bf16x2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv);
-                        v4.z = cvt_bf16x2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv);
-                        v4.w = cvt_bf16x2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv);
-                        dst[c * 4 + k] = v4;
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(t_row + C::col_o(t) + 64 * hf + c * 32, r);
+                        tmem_wait_ld();
+                        #pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            *reinterpret_cast<uint4*>(stg + (((4 * c + k) ^ (lane & 7)) << 4)) = cvt8(r + 8 * k);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_4d(&tm_o, sbase + stg_off, 64 * hf, h, qt * C::BM + 32 * (warp & 3), b);
+                        bulk_commit();
+                        bulk_wait_read();     // before the CTA's shared memory goes away
+                    }
+                    __syncwarp();
+                } else {
+                    const long long orow = b * args.o_sb + (static_cast<long long>(qt) * C::BM + row) * args.o_sn +
+                                           h * args.o_sh;
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + orow + 64 * hf);
+                    #pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(t_row + C::col_o(t) + 64 * hf + c * 32, r);
+                        tmem_wait_ld();
+                        #pragma unroll
+                        for (int k = 0; k < 4; ++k) dst[c * 4 + k] = cvt8(r + 8 * k);
                     }
                 }
             }

@@ -102,7 +102,13 @@ struct Fwd4Cfg {
     static constexpr int B_MD = B_TD + 1;
     static constexpr int B_MH = B_MD + 2;
     static constexpr int NBAR = B_MH + 8;
-    static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16;
+    // O staging for bulk tensor stores (d_qk = 128 only: at 192 the ring
+    // leaves no room): per correction warp 32 rows x 64 columns of BF16, 128-byte
+    // swizzle, 1024-aligned; a tile's 64-column halves pass through in turn
+    static constexpr bool OST = DQK == 128;
+    static constexpr int OST_WARP = 32 * 128;
+    static constexpr int OFF_OST = (OFF_BAR + NBAR * 8 + 16 + 1023) / 1024 * 1024;
+    static constexpr int SMEM_BYTES = OST ? OFF_OST + 4 * OST_WARP : OFF_BAR + NBAR * 8 + 16;
     static constexpr int SMEM_ALLOC = SMEM_BYTES;   // base is 1024-aligned (checked)
     static constexpr uint32_t COL_S0 = 0, COL_O = 256, COL_P0 = 384, COL_L = 480;
     static constexpr uint32_t COL_SFA0 = 496, COL_SFB = 508;
@@ -192,7 +198,8 @@ __device__ __forceinline__ void fwd4_next(BlockCur& c, const FwdArgs& a, int T) 
 template <int DQK, int LEAN>
 __global__ void __launch_bounds__(Fwd4Cfg<DQK>::THREADS, 1)
 zyfa_fwd4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const FwdArgs args) {
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                 const FwdArgs args) {
     using C = Fwd4Cfg<DQK>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_u32(smem);
@@ -436,20 +443,50 @@ zyfa_fwd4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // LSE of the rounded weights: l is relative to the final running
                 // max and carries the 2^sigma shift (Sec. IV-B3)
                 if (args.lse) args.lse[lse_at(t)] = logf(l) + (m_fin - kSigma) * 0.6931471805599453f;
-                uint4* dst = out_row(t);
-                #pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(t_row + C::COL_O + c * 32, r);
-                    tmem_wait_ld();
-                    #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint4 v4;
-                        v4.x = cvt_bf16x2(__uint_as_float(r[8 * k + 0]) * inv, __uint_as_float(r[8 * k + 1]) * inv);
-                        v4.y = cvt_bf16x2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv);
-                        v4.z = cvt_bf16x2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv);
-                        v4.w = cvt_bf16x2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv);
-                        dst[c * 4 + k] = v4;
+                auto cvt8 = [&](const uint32_t* r) -> uint4 {
+                    uint4 v4;
+                    v4.x = cvt_bf16x2(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv);
+                    v4.y = cvt_bf16x2(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv);
+                    v4.z = cvt_bf16x2(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv);
+                    v4.w = cvt_bf16x2(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
+                    return v4;
+                };
+                if (C::OST && args.o_tma) {
+                    // each 64-column half: the warp's 32 rows into its staging
+                    // (16-byte chunk j of row r at position j ^ (r & 7)), then one
+                    // bulk tensor store; the warp goes on without waiting for it
+                    uint8_t* stg = smem + C::OFF_OST + q4 * C::OST_WARP + lane * 128;
+                    #pragma unroll 1
+                    for (int hf = 0; hf < 2; ++hf) {
+                        // the staging's previous store has read it
+                        if (lane == 0) bulk_wait_read();
+                        __syncwarp();
+                        #pragma unroll 1
+                        for (int c = 0; c < 2; ++c) {
+                            uint32_t r[32];
+                            tmem_ld32(t_row + C::COL_O + hf * 64 + c * 32, r);
+                            tmem_wait_ld();
+                            #pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                *reinterpret_cast<uint4*>(stg + (((4 * c + k) ^ (lane & 7)) << 4)) = cvt8(r + 8 * k);
+                        }
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_4d(&tm_o, smem_u32(smem + C::OFF_OST + q4 * C::OST_WARP), 64 * hf, t.h,
+                                         t.qt * C::BM + 32 * q4, t.b);
+                            bulk_commit();
+                        }
+                    }
+                } else {
+                    uint4* dst = out_row(t);
+                    #pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(t_row + C::COL_O + c * 32, r);
+                        tmem_wait_ld();
+                        #pragma unroll
+                        for (int k = 0; k < 4; ++k) dst[c * 4 + k] = cvt8(r + 8 * k);
                     }
                 }
                 return true;
@@ -515,6 +552,9 @@ zyfa_fwd4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 ++tq;
             }
             if (ok && pend) ok = epilogue(pt, pm, tq - 1);
+            // the output's bulk stores complete before the CTA exits
+            if (C::OST && args.o_tma && lane == 0) bulk_wait_all();
+            __syncwarp();
             tc_fence_before();
         } else if (warp == C::WARP_TMA) {
             // ------------------------------------------------------------ producer

@@ -38,7 +38,7 @@ struct Strides {
 // 4-D map over a [B, N, H, d] tensor with strides st: dims (d, H, N, B), box
 // (inner, 1, 128, 1).
 bool make_map(CUtensorMap* m, const void* base, bool bf16, int d, int H, int N, int B,
-              const Strides& st, int box_inner, CUtensorMapSwizzle swz) {
+              const Strides& st, int box_inner, CUtensorMapSwizzle swz, int box_rows = 128) {
     auto enc = encode_fn();
     if (!enc) return false;
     const uint64_t esz = bf16 ? 2 : 1;
@@ -46,7 +46,7 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, int d, int H, int N, 
                           static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
     cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.h) * esz, static_cast<cuuint64_t>(st.n) * esz,
                              static_cast<cuuint64_t>(st.b) * esz};
-    cuuint32_t box[4] = {static_cast<cuuint32_t>(box_inner), 1, 128, 1};
+    cuuint32_t box[4] = {static_cast<cuuint32_t>(box_inner), 1, static_cast<cuuint32_t>(box_rows), 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 4,
                      const_cast<void*>(base), dims, strides, box, estr,
@@ -123,13 +123,18 @@ int launch3(const void* q, const void* k, const void* v, const FwdArgs& a, const
     if (!make_map(&tk, k, false, DQK, a.Hkv, a.N, a.B, L.k, C::CB, swz)) return ZYFA_ERR_CUDA;
     if (!make_map(&tv, v, false, C::DV, a.Hkv, a.N, a.B, L.v, 128, CU_TENSOR_MAP_SWIZZLE_128B))
         return ZYFA_ERR_CUDA;
+    // O leaves through shared memory and bulk tensor stores (32 rows x 64
+    // columns per box) where the output strides allow a tensor map
+    CUtensorMap to{};
+    FwdArgs ao = a;
+    ao.o_tma = make_map(&to, a.out, true, C::DV, a.Hq, a.N, a.B, L.o, 64, CU_TENSOR_MAP_SWIZZLE_128B, 32) ? 1 : 0;
     auto kern = a.p_mode == ZYFA_P_LEAN ? zyfa_fwd3_kernel<DQK, 1> : zyfa_fwd3_kernel<DQK, 0>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
         cudaSuccess)
         return ZYFA_ERR_CUDA;
     const int T = a.N / C::BM;
     const unsigned grid = static_cast<unsigned>(a.B) * a.Hq * ((T + 1) / 2);
-    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, a);
+    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, to, ao);
     return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
 }
 
@@ -146,6 +151,13 @@ int launch4(const void* q, const void* k, const void* v, const FwdArgs& a, const
     if (!make_map(&tk, k, false, DQK, a.Hkv, a.N, a.B, L.k, C::CB, swz)) return ZYFA_ERR_CUDA;
     if (!make_map(&tv, v, false, C::DV, a.Hkv, a.N, a.B, L.v, 128, CU_TENSOR_MAP_SWIZZLE_128B))
         return ZYFA_ERR_CUDA;
+    // O tiles leave through shared memory and bulk tensor stores (32 rows x
+    // 64 columns per box, 128-byte swizzle) where the kernel has room for the
+    // staging and the output strides allow a tensor map; else row stores
+    CUtensorMap to{};
+    FwdArgs ao = a;
+    ao.o_tma = C::OST && make_map(&to, a.out, true, C::DV, a.Hq, a.N, a.B, L.o, 64,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, 32) ? 1 : 0;
     auto kern = a.p_mode == ZYFA_P_LEAN ? zyfa_fwd4_kernel<DQK, 1> : zyfa_fwd4_kernel<DQK, 0>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
         cudaSuccess)
@@ -159,7 +171,7 @@ int launch4(const void* q, const void* k, const void* v, const FwdArgs& a, const
     // the kernel keeps the grid's mixed-radix digits in bytes (grid <= 255)
     const long long cap = sms < 255 ? sms : 255;
     const unsigned grid = static_cast<unsigned>(items < cap ? items : cap);
-    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, a);
+    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, to, ao);
     return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
 }
 
