@@ -60,10 +60,6 @@ struct FwdArgs {
     // is every key.  Read by the kernels of fwd.cuh and fwd3.cuh.
     int kb0 = 0;
     int kb1 = 1 << 30;
-    // 1: out is also described by the tensor map the kernel receives for it
-    // (16-byte strides), so a kernel that stages O tiles in shared memory may
-    // write them with bulk tensor stores; 0: 16-byte stores per row
-    int o_tma = 0;
 };
 
 // FP8: e4m3 V and probabilities (the PV path); QK16: Q and K in BF16 (the

@@ -527,7 +527,7 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     v4.w = cvt_bf16x2(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
                     return v4;
                 };
-                if (args.o_tma) {
+                {
                     // through shared memory and one bulk tensor store per warp
                     // (32 rows x 64 columns, 128-byte swizzle: 16-byte chunk j of
                     // row r at position j ^ (r & 7)); the staging is the tile's
@@ -552,18 +552,6 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         bulk_wait_read();     // before the CTA's shared memory goes away
                     }
                     __syncwarp();
-                } else {
-                    const long long orow = b * args.o_sb + (static_cast<long long>(qt) * C::BM + row) * args.o_sn +
-                                           h * args.o_sh;
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.out) + orow + 64 * hf);
-                    #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(t_row + C::col_o(t) + 64 * hf + c * 32, r);
-                        tmem_wait_ld();
-                        #pragma unroll
-                        for (int k = 0; k < 4; ++k) dst[c * 4 + k] = cvt8(r + 8 * k);
-                    }
                 }
             }
         } else if (t == 0 || has_b) {

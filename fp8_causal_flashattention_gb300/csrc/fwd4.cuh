@@ -451,7 +451,7 @@ zyfa_fwd4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     v4.w = cvt_bf16x2(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
                     return v4;
                 };
-                if (C::OST && args.o_tma) {
+                if constexpr (C::OST) {
                     // each 64-column half: the warp's 32 rows into its staging
                     // (16-byte chunk j of row r at position j ^ (r & 7)), then one
                     // bulk tensor store; the warp goes on without waiting for it
@@ -553,7 +553,7 @@ zyfa_fwd4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             if (ok && pend) ok = epilogue(pt, pm, tq - 1);
             // the output's bulk stores complete before the CTA exits
-            if (C::OST && args.o_tma && lane == 0) bulk_wait_all();
+            if (C::OST && lane == 0) bulk_wait_all();
             __syncwarp();
             tc_fence_before();
         } else if (warp == C::WARP_TMA) {

@@ -88,6 +88,7 @@ int check_strides(const Layout4& L, int qk_esz, int v_esz) {
     for (long long x : o) {
         if (x <= 0) return ZYFA_ERR_SHAPE;
         if ((x * 2) % 16 != 0) return ZYFA_ERR_ALIGN;
+        if (x * 2 >= (1ll << 40)) return ZYFA_ERR_SHAPE;   // the FP8 kernels store O through a tensor map
     }
     return ZYFA_OK;
 }
@@ -124,17 +125,17 @@ int launch3(const void* q, const void* k, const void* v, const FwdArgs& a, const
     if (!make_map(&tv, v, false, C::DV, a.Hkv, a.N, a.B, L.v, 128, CU_TENSOR_MAP_SWIZZLE_128B))
         return ZYFA_ERR_CUDA;
     // O leaves through shared memory and bulk tensor stores (32 rows x 64
-    // columns per box) where the output strides allow a tensor map
-    CUtensorMap to{};
-    FwdArgs ao = a;
-    ao.o_tma = make_map(&to, a.out, true, C::DV, a.Hq, a.N, a.B, L.o, 64, CU_TENSOR_MAP_SWIZZLE_128B, 32) ? 1 : 0;
+    // columns per box, 128-byte swizzle)
+    CUtensorMap to;
+    if (!make_map(&to, a.out, true, C::DV, a.Hq, a.N, a.B, L.o, 64, CU_TENSOR_MAP_SWIZZLE_128B, 32))
+        return ZYFA_ERR_CUDA;
     auto kern = a.p_mode == ZYFA_P_LEAN ? zyfa_fwd3_kernel<DQK, 1> : zyfa_fwd3_kernel<DQK, 0>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
         cudaSuccess)
         return ZYFA_ERR_CUDA;
     const int T = a.N / C::BM;
     const unsigned grid = static_cast<unsigned>(a.B) * a.Hq * ((T + 1) / 2);
-    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, to, ao);
+    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, to, a);
     return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
 }
 
@@ -152,12 +153,11 @@ int launch4(const void* q, const void* k, const void* v, const FwdArgs& a, const
     if (!make_map(&tv, v, false, C::DV, a.Hkv, a.N, a.B, L.v, 128, CU_TENSOR_MAP_SWIZZLE_128B))
         return ZYFA_ERR_CUDA;
     // O tiles leave through shared memory and bulk tensor stores (32 rows x
-    // 64 columns per box, 128-byte swizzle) where the kernel has room for the
-    // staging and the output strides allow a tensor map; else row stores
+    // 64 columns per box, 128-byte swizzle) at d_qk = 128; at 192 the kernel
+    // has no room for the staging and writes rows
     CUtensorMap to{};
-    FwdArgs ao = a;
-    ao.o_tma = C::OST && make_map(&to, a.out, true, C::DV, a.Hq, a.N, a.B, L.o, 64,
-                                  CU_TENSOR_MAP_SWIZZLE_128B, 32) ? 1 : 0;
+    if (C::OST && !make_map(&to, a.out, true, C::DV, a.Hq, a.N, a.B, L.o, 64, CU_TENSOR_MAP_SWIZZLE_128B, 32))
+        return ZYFA_ERR_CUDA;
     auto kern = a.p_mode == ZYFA_P_LEAN ? zyfa_fwd4_kernel<DQK, 1> : zyfa_fwd4_kernel<DQK, 0>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
         cudaSuccess)
@@ -171,7 +171,7 @@ int launch4(const void* q, const void* k, const void* v, const FwdArgs& a, const
     // the kernel keeps the grid's mixed-radix digits in bytes (grid <= 255)
     const long long cap = sms < 255 ? sms : 255;
     const unsigned grid = static_cast<unsigned>(items < cap ? items : cap);
-    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, to, ao);
+    kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, to, a);
     return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
 }
 

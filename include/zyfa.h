@@ -204,7 +204,8 @@ int zyfa_quantize_noalloc(const void* x, const float* signs, int smooth, float s
  *             of q, k, v and out.  BHSD is {H N d, d, N d} for each.
  * Each stride must be positive; q, k and v strides times the element size
  * must be multiples of 16 bytes (TMA) and below 2^40 bytes, out strides
- * multiples of 8 elements.  ZYFA_ERR_SHAPE / ZYFA_ERR_ALIGN otherwise.
+ * multiples of 8 elements and below 2^39 elements (the FP8 kernels write out
+ * through a tensor map too).  ZYFA_ERR_SHAPE / ZYFA_ERR_ALIGN otherwise.
  * Everything else as zyfa_fwd_ex (lse stays [B, Hq, N] contiguous).
  */
 int zyfa_fwd_strided(const void* q, const void* k, const void* v,

@@ -145,6 +145,7 @@ def _bshd(B, N, H, d):
     ("v", [0, 128, 128], Z.ZYFA_ERR_SHAPE),
     ("o", [256 * 2 * 128, 2 * 128, 124], Z.ZYFA_ERR_ALIGN),     # 248 B: not 16-byte aligned
     ("q", [1 << 40, 256, 128], Z.ZYFA_ERR_SHAPE),                # byte stride >= 2^40
+    ("o", [1 << 39, 256, 128], Z.ZYFA_ERR_SHAPE),                # 2^40 bytes: the output's tensor map
 ])
 def test_strided_argument_errors(lib, which, bad, want):
     st = {"q": _bshd(1, 256, 2, 128), "k": _bshd(1, 256, 1, 128), "v": _bshd(1, 256, 1, 128),
