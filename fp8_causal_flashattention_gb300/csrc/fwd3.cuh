@@ -132,25 +132,43 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int nb1 = has_b ? nblocks(qt0 + 1) : 0;
     const int nblk = nb0 > nb1 ? nb0 : nb1;
 
-    if (threadIdx.x == 0) {
-        mbar_init(BAR(B_QF), 1);
-        for (int s = 0; s < C::NST; ++s) {
-            mbar_init(BAR(B_KF + s), 1);
-            mbar_init(BAR(B_VF + s), 1);
-            mbar_init(BAR(B_KE + s), 2);          // one commit per PV issuer
+    auto load_kv = [&](int i) {
+        const int st = i % C::NST;
+        mbar_expect_tx_elect(BAR(B_KF + st), C::K_BYTES);
+        #pragma unroll
+        for (int c = 0; c < C::NCH; ++c)
+            tma_load_4d_elect(sbase + C::OFF_K + st * C::K_BYTES + c * (C::BN * C::CB), &tm_k,
+                              BAR(B_KF + st), c * C::CB, g, (args.kb0 + i) * C::BN, b);
+        mbar_expect_tx_elect(BAR(B_VF + st), C::V_BYTES);
+        tma_load_4d_elect(sbase + C::OFF_V + st * C::V_BYTES, &tm_v, BAR(B_VF + st), 0, g,
+                          (args.kb0 + i) * C::BN, b);
+    };
+    if (warp == 0) {
+        // one barrier per lane; then Q and the first K/V blocks are requested
+        // at once, before the rest of the CTA is set up
+        for (int i = lane; i < C::NBAR; i += 32) {
+            uint32_t n = 1;                           // q_full, k_full, v_full, s_full, o_done, fin, mma_done
+            if (i >= B_KE && i < B_KE + C::NST) n = 2;   // one commit per PV issuer
+            else if (i == B_SX || i == B_SX + 1) n = 128;
+            else if (i == B_PF || i == B_PF + 1 || i == B_X || i == B_X + 1) n = 256;   // both warpgroups of the tile
+            mbar_init(BAR(i), n);
         }
-        for (int t = 0; t < 4; ++t) mbar_init(BAR(B_SF + t), 1);
-        for (int t = 0; t < 2; ++t) {
-            mbar_init(BAR(B_SX + t), 128);
-            mbar_init(BAR(B_PF + t), 256);           // both warpgroups of the tile
-            mbar_init(BAR(B_OD + t), 1);
-            mbar_init(BAR(B_FIN + t), 1);
-        }
-        for (int k = 0; k < 4; ++k) mbar_init(BAR(B_MD + k), 1);
-        mbar_init(BAR(B_X), 256);
-        mbar_init(BAR(B_X + 1), 256);
-        *abort_flag = 0;
+        if (lane == 0) *abort_flag = 0;
         fence_mbar_init();
+        __syncwarp();
+        if (nblk > 0) {                               // (nothing, not even Q, when no block)
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_expect_tx_elect(BAR(B_QF), (has_b ? 2 : 1) * C::Q_BYTES);
+            for (int u = 0; u < (has_b ? 2 : 1); ++u) {
+                #pragma unroll
+                for (int c = 0; c < C::NCH; ++c)
+                    tma_load_4d_elect(sbase + C::OFF_Q + u * C::Q_BYTES + c * (C::BM * C::CB), &tm_q,
+                                      BAR(B_QF), c * C::CB, h, (qt0 + u) * C::BM, b);
+            }
+            for (int i = 0; i < nblk && i < C::NST; ++i) load_kv(i);
+        }
     }
     if (warp == C::WARP_QK) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -247,31 +265,8 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tc_commit_elect(BAR(B_KE + st));
             if (!(i < nb0 && i < nb1)) tc_commit_elect(BAR(B_KE + st));
         };
-        auto load_kv = [&](int i) {
-            const int st = i % C::NST;
-            mbar_expect_tx_elect(BAR(B_KF + st), C::K_BYTES);
-            #pragma unroll
-            for (int c = 0; c < C::NCH; ++c)
-                tma_load_4d_elect(sbase + C::OFF_K + st * C::K_BYTES + c * (C::BN * C::CB), &tm_k,
-                                  BAR(B_KF + st), c * C::CB, g, (args.kb0 + i) * C::BN, b);
-            mbar_expect_tx_elect(BAR(B_VF + st), C::V_BYTES);
-            tma_load_4d_elect(sbase + C::OFF_V + st * C::V_BYTES, &tm_v, BAR(B_VF + st), 0, g,
-                              (args.kb0 + i) * C::BN, b);
-        };
-        int li = 0;                                  // next K/V block to load (issuer A)
-        if (t == 0 && nblk > 0) {                    // (nothing, not even Q, when no block)
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            mbar_expect_tx_elect(BAR(B_QF), (has_b ? 2 : 1) * C::Q_BYTES);
-            for (int u = 0; u < (has_b ? 2 : 1); ++u) {
-                #pragma unroll
-                for (int c = 0; c < C::NCH; ++c)
-                    tma_load_4d_elect(sbase + C::OFF_Q + u * C::Q_BYTES + c * (C::BM * C::CB), &tm_q,
-                                      BAR(B_QF), c * C::CB, h, (qt0 + u) * C::BM, b);
-            }
-            for (; li < nblk && li < C::NST; ++li) load_kv(li);
-        }
+        // next K/V block to load (issuer A; warp 0 requested the first ones)
+        int li = nblk < C::NST ? nblk : C::NST;
         int pj = 0;
         bool ok = true;
         if (t == 1) {
