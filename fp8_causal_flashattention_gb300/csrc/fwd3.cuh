@@ -51,20 +51,27 @@ struct Fwd3Cfg {
     static constexpr int K_BYTES = BN * DQK;
     static constexpr int V_BYTES = BN * DV;
     static constexpr int P_BYTES = BM * BN;         // one tile, K-major, 128-byte swizzle
-    static constexpr int NST = DQK == 128 ? 4 : 2;
+    // K/V ring.  d_qk = 128: one ring of 4 stages, a stage freed by the PVs of
+    // its block.  d_qk = 192 (two 24 KB Q tiles): separate rings, a K stage
+    // freed once both tiles' QKs of its block have completed and a V stage
+    // after their PVs, so that 2 K + 4 V stages fit (one ring had room for 2).
+    static constexpr bool SPLIT = DQK == 192;
+    static constexpr int NSK = SPLIT ? 2 : 4;
+    static constexpr int NSV = 4;
     static constexpr int QK_STEPS = DQK / 32;       // 32 bytes of K per MMA
     static constexpr int PV_STEPS = BN / 32;
     static constexpr int ONES_BYTES = 2048;         // 16 x 128 e4m3 ones
     static constexpr int OFF_Q = 0;                 // tiles A, B
     static constexpr int OFF_K = OFF_Q + 2 * Q_BYTES;
-    static constexpr int OFF_V = OFF_K + NST * K_BYTES;
-    static constexpr int OFF_P = OFF_V + NST * V_BYTES;
+    static constexpr int OFF_V = OFF_K + NSK * K_BYTES;
+    static constexpr int OFF_P = OFF_V + NSV * V_BYTES;
     static constexpr int OFF_ONES = OFF_P + 4 * P_BYTES;   // [tile][slot]
     static constexpr int OFF_BAR = OFF_ONES + ONES_BYTES;
-    // q_full, k_full[NST], v_full[NST], kv_empty[NST], s_full[2], s_free[2],
-    // p_full[2], o_done[2], fin[2], mma_done[4]; then the TMEM slot and the
-    // abort flag
-    static constexpr int NBAR = 1 + 3 * NST + 12 + 4 + 2;
+    // q_full, k_full[NSK], v_full[NSV], k_empty[NSK] (one ring: the stage's
+    // empty barrier), v_empty[NSV] (split rings only), s_full[2][2],
+    // s_free[2], p_full[2], o_done[2], fin[2], mma_done[4], exchange[2]; then
+    // the TMEM slot and the abort flag
+    static constexpr int NBAR = 1 + NSK + NSV + NSK + (SPLIT ? NSV : 0) + 18;
     static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16;
     static constexpr int SMEM_ALLOC = SMEM_BYTES;
     static __host__ __device__ constexpr uint32_t col_s(int t) { return 64u * t; }
@@ -93,11 +100,13 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
     const uint32_t bar0 = smem_u32(bars);
     auto BAR = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
-    const int B_QF = 0, B_KF = 1, B_VF = 1 + C::NST, B_KE = 1 + 2 * C::NST;
+    const int B_QF = 0, B_KF = 1, B_VF = B_KF + C::NSK, B_KE = B_VF + C::NSV;
+    const int B_VE = C::SPLIT ? B_KE + C::NSK : B_KE;     // one ring: V's stage is K's
+    const int B_SF = B_KE + C::NSK + (C::SPLIT ? C::NSV : 0);
     // s_full: [tile][half], one phase per block, so each half's warpgroup
     // waits on a barrier of its own (a shared one would run up to three
     // phases ahead of the slower warpgroup, beyond what a parity wait tells)
-    const int B_SF = 1 + 3 * C::NST, B_SX = B_SF + 4, B_PF = B_SX + 2, B_OD = B_PF + 2;
+    const int B_SX = B_SF + 4, B_PF = B_SX + 2, B_OD = B_PF + 2;
     const int B_FIN = B_OD + 2, B_MD = B_FIN + 2;   // B_MD: [4], one per issuer warp
     const int B_X = B_MD + 4;                        // [2]: a tile's half maxima exchanged
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
@@ -132,13 +141,16 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int nb1 = has_b ? nblocks(qt0 + 1) : 0;
     const int nblk = nb0 > nb1 ? nb0 : nb1;
 
-    auto load_kv = [&](int i) {
-        const int st = i % C::NST;
+    auto load_k = [&](int i) {
+        const int st = i % C::NSK;
         mbar_expect_tx_elect(BAR(B_KF + st), C::K_BYTES);
         #pragma unroll
         for (int c = 0; c < C::NCH; ++c)
             tma_load_4d_elect(sbase + C::OFF_K + st * C::K_BYTES + c * (C::BN * C::CB), &tm_k,
                               BAR(B_KF + st), c * C::CB, g, (args.kb0 + i) * C::BN, b);
+    };
+    auto load_v = [&](int i) {
+        const int st = i % C::NSV;
         mbar_expect_tx_elect(BAR(B_VF + st), C::V_BYTES);
         tma_load_4d_elect(sbase + C::OFF_V + st * C::V_BYTES, &tm_v, BAR(B_VF + st), 0, g,
                           (args.kb0 + i) * C::BN, b);
@@ -148,7 +160,7 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // at once, before the rest of the CTA is set up
         for (int i = lane; i < C::NBAR; i += 32) {
             uint32_t n = 1;                           // q_full, k_full, v_full, s_full, o_done, fin, mma_done
-            if (i >= B_KE && i < B_KE + C::NST) n = 2;   // one commit per PV issuer
+            if (i >= B_KE && i < B_SF) n = 2;     // one commit per QK (split K) or PV issuer
             else if (i == B_SX || i == B_SX + 1) n = 128;
             else if (i == B_PF || i == B_PF + 1 || i == B_X || i == B_X + 1) n = 256;   // both warpgroups of the tile
             mbar_init(BAR(i), n);
@@ -167,7 +179,10 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tma_load_4d_elect(sbase + C::OFF_Q + u * C::Q_BYTES + c * (C::BM * C::CB), &tm_q,
                                       BAR(B_QF), c * C::CB, h, (qt0 + u) * C::BM, b);
             }
-            for (int i = 0; i < nblk && i < C::NST; ++i) load_kv(i);
+            for (int i = 0; i < nblk && i < C::NSV; ++i) {
+                if (i < C::NSK) load_k(i);
+                load_v(i);
+            }
         }
     }
     if (warp == C::WARP_QK) {
@@ -194,14 +209,16 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // read (s_free); QK(j, 1) needs half 0 of block j read.  The softmax
         // releases two halves per block, so s_free completes phases 2j (half
         // 0) and 2j + 1 (half 1); each waited phase is the next one (its
-        // successor needs a QK this warp has not issued yet).
+        // successor needs a QK this warp has not issued yet).  A K stage is
+        // released by one commit from each QK issuer after its block's second
+        // half (split rings); the only user of a block commits twice.
         const int t = warp - C::WARP_QK;
         const int nbt = t ? nb1 : nb0;
         constexpr uint32_t kQK = idesc_dense(kFmtE4M3, kFmtE4M3, 0, 0, 128, C::HN);
         const uint64_t dq = smem_desc(sbase + C::OFF_Q + t * C::Q_BYTES, 16, 8 * C::CB, C::SWZ);
         const uint64_t dk0 = smem_desc(sbase + C::OFF_K, 16, 8 * C::CB, C::SWZ);
         auto issue_qk = [&](int i, int hf) {
-            const int st = i % C::NST;
+            const int st = i % C::NSK;
             const uint64_t dk = dk0 + static_cast<uint64_t>((st * C::K_BYTES + hf * C::HN * C::CB) >> 4);
             #pragma unroll
             for (int kk = 0; kk < C::QK_STEPS; ++kk) {
@@ -217,12 +234,16 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         bool ok = nbt > 0 && wait_warp(B_QF, 0, 22);
         for (int j = 0; ok && j < nbt; ++j) {
             if (j > 0 && !(ok = wait_warp(B_SX + t, 1, 31))) break;       // half 1 of j-1 read
-            if (!(ok = wait_warp(B_KF + j % C::NST, (j / C::NST) & 1, 27))) break;
+            if (!(ok = wait_warp(B_KF + j % C::NSK, (j / C::NSK) & 1, 27))) break;
             tc_fence_after();
             issue_qk(j, 0);
             if (!(ok = wait_warp(B_SX + t, 0, 28))) break;                 // half 0 of j read
             tc_fence_after();
             issue_qk(j, 1);
+            if constexpr (C::SPLIT) {
+                tc_commit_elect(BAR(B_KE + j % C::NSK));
+                if (!(j < nb0 && j < nb1)) tc_commit_elect(BAR(B_KE + j % C::NSK));
+            }
         }
         tc_commit_elect(BAR(B_MD + t));
         unsigned long long t0 = globaltimer();
@@ -232,17 +253,17 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         // ------------------------------------------------------------ PV issuers
         // PV(t, j) needs P_j (p_full) and V_j.  The softmax publishes P_j only
         // after PV(t, j-1) has completed (o_done), so p_full is never more than
-        // one phase ahead.  o_done(t) completes one phase per PV(t, j).  A K/V
-        // stage is released by one commit from each PV issuer; the only user
-        // of a block (the last causal block, or a CTA with one tile) commits
-        // twice.  Issuer A also loads Q and the K/V ring with TMA: it polls
-        // both kinds of work, so neither waits for the other.
+        // one phase ahead.  o_done(t) completes one phase per PV(t, j).  A V
+        // (one ring: K/V) stage is released by one commit from each PV issuer;
+        // the only user of a block (the last causal block, or a CTA with one
+        // tile) commits twice.  Issuer A also loads the rings with TMA: it
+        // polls loads and PVs, so neither waits for the other.
         const int t = warp - C::WARP_PV;
         const int nbt = t ? nb1 : nb0;
         const uint64_t dv0 = smem_desc(sbase + C::OFF_V, 1024, 1024, kSwizzle128B);
         const uint64_t d10 = smem_desc(sbase + C::OFF_ONES, 16, 1024, kSwizzle128B);
         auto issue_pv = [&](int i) {
-            const int st = i % C::NST;
+            const int st = i % C::NSV;
             const uint64_t dp = smem_desc(sbase + C::OFF_P + (2 * t + (i & 1)) * C::P_BYTES, 16, 1024,
                                           kSwizzle128B);
             const uint64_t dv = dv0 + static_cast<uint64_t>((st * C::V_BYTES) >> 4);
@@ -262,37 +283,45 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             tc_commit_elect(BAR(B_OD + t));
             if (i == nbt - 1) tc_commit_elect(BAR(B_FIN + t));
-            tc_commit_elect(BAR(B_KE + st));
-            if (!(i < nb0 && i < nb1)) tc_commit_elect(BAR(B_KE + st));
+            tc_commit_elect(BAR(B_VE + st));
+            if (!(i < nb0 && i < nb1)) tc_commit_elect(BAR(B_VE + st));
         };
-        // next K/V block to load (issuer A; warp 0 requested the first ones)
-        int li = nblk < C::NST ? nblk : C::NST;
+        // next K and V blocks to load (issuer A; warp 0 requested the first ones)
+        int lk = nblk < C::NSK ? nblk : C::NSK;
+        int lv = nblk < C::NSV ? nblk : C::NSV;
         int pj = 0;
         bool ok = true;
         if (t == 1) {
             // no loads to interleave: block on the barriers
             for (; ok && pj < nbt; ++pj) {
                 if (!(ok = wait_warp(B_PF + 1, pj & 1, 29))) break;
-                if (!(ok = wait_warp(B_VF + pj % C::NST, (pj / C::NST) & 1, 30))) break;
+                if (!(ok = wait_warp(B_VF + pj % C::NSV, (pj / C::NSV) & 1, 30))) break;
                 tc_fence_after();
                 issue_pv(pj);
             }
         }
         unsigned long long t_prog = globaltimer();
-        while (ok && (pj < nbt || (t == 0 && li < nblk))) {
+        while (ok && (pj < nbt || (t == 0 && lv < nblk))) {
             bool did = false;
-            if (t == 0 && li < nblk) {
-                const int st = li % C::NST;
-                if (__all_sync(0xffffffffu, mbar_test(BAR(B_KE + st), ((li / C::NST) - 1) & 1))) {
-                    load_kv(li);
-                    ++li;
+            if constexpr (C::SPLIT) {
+                if (t == 0 && lk < nblk &&
+                    __all_sync(0xffffffffu, mbar_test(BAR(B_KE + lk % C::NSK), ((lk / C::NSK) - 1) & 1))) {
+                    load_k(lk);
+                    ++lk;
                     did = true;
                 }
             }
+            if (t == 0 && lv < nblk &&
+                __all_sync(0xffffffffu, mbar_test(BAR(B_VE + lv % C::NSV), ((lv / C::NSV) - 1) & 1))) {
+                if constexpr (!C::SPLIT) load_k(lv);        // one ring: K and V of a block together
+                load_v(lv);
+                ++lv;
+                did = true;
+            }
             if (pj < nbt) {
-                const int st = pj % C::NST;
+                const int st = pj % C::NSV;
                 const bool rdy = mbar_test(BAR(B_PF + t), pj & 1) &&
-                                 mbar_test(BAR(B_VF + st), (pj / C::NST) & 1);
+                                 mbar_test(BAR(B_VF + st), (pj / C::NSV) & 1);
                 if (__all_sync(0xffffffffu, rdy)) {
                     tc_fence_after();
                     issue_pv(pj);
@@ -309,15 +338,17 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // blocks before its QK), instead of spinning on the issue slots
             // that this SM sub-partition's softmax warps need.
             if (pj < nbt) {
-                const int st = pj % C::NST;
+                const int st = pj % C::NSV;
                 const bool pf = __all_sync(0xffffffffu, mbar_test(BAR(B_PF + t), pj & 1));
                 (void)__all_sync(0xffffffffu,
-                                 pf ? mbar_try_for(BAR(B_VF + st), (pj / C::NST) & 1, kIdleWaitNs)
+                                 pf ? mbar_try_for(BAR(B_VF + st), (pj / C::NSV) & 1, kIdleWaitNs)
                                     : mbar_try_for(BAR(B_PF + t), pj & 1, kIdleWaitNs));
+            } else if (C::SPLIT && lk < nblk) {
+                (void)__all_sync(0xffffffffu, mbar_try_for(BAR(B_KE + lk % C::NSK), ((lk / C::NSK) - 1) & 1,
+                                                           kIdleWaitNs));
             } else {
-                const int st = li % C::NST;
-                (void)__all_sync(0xffffffffu,
-                                 mbar_try_for(BAR(B_KE + st), ((li / C::NST) - 1) & 1, kIdleWaitNs));
+                (void)__all_sync(0xffffffffu, mbar_try_for(BAR(B_VE + lv % C::NSV), ((lv / C::NSV) - 1) & 1,
+                                                           kIdleWaitNs));
             }
             if (*abort_flag) {
                 ok = false;
@@ -332,12 +363,14 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         while (!mbar_try(BAR(B_MD + 2 + t), 0) && globaltimer() - t0 < kWaitBudgetNs) {}
         if (t == 0 && *abort_flag) {
             // let the loads still in flight land before the CTA exits
-            for (int i = li - C::NST < 0 ? 0 : li - C::NST; i < li; ++i) {
-                const int st = i % C::NST;
-                const uint32_t ph = (i / C::NST) & 1;
+            if (!C::SPLIT) lk = lv;
+            for (int i = lk - C::NSK < 0 ? 0 : lk - C::NSK; i < lk; ++i) {
                 unsigned long long t1 = globaltimer();
-                while (!mbar_try(BAR(B_KF + st), ph) && globaltimer() - t1 < kWaitBudgetNs) {}
-                while (!mbar_try(BAR(B_VF + st), ph) && globaltimer() - t1 < kWaitBudgetNs) {}
+                while (!mbar_try(BAR(B_KF + i % C::NSK), (i / C::NSK) & 1) && globaltimer() - t1 < kWaitBudgetNs) {}
+            }
+            for (int i = lv - C::NSV < 0 ? 0 : lv - C::NSV; i < lv; ++i) {
+                unsigned long long t1 = globaltimer();
+                while (!mbar_try(BAR(B_VF + i % C::NSV), (i / C::NSV) & 1) && globaltimer() - t1 < kWaitBudgetNs) {}
             }
         }
         __syncwarp();

@@ -196,18 +196,22 @@ int launch(const void* q, const void* k, const void* v, const FwdArgs& a, const 
     return cudaGetLastError() == cudaSuccess ? ZYFA_OK : ZYFA_ERR_CUDA;
 }
 
-// The FP8 forward's kernel per mode and length, by measurement on GB300
-// (outputs bit-identical between the two): at d_qk = 128 the two-tile kernel
-// (fwd3.cuh) for Lean P beyond 2048 keys and exact P beyond 4096 (d128 N =
-// 32K: Lean 1866 against 1609 TFLOP/s, exact 1789 against 1667), the
-// persistent kernel over causal pairs (fwd4.cuh) below that, where the
-// persistent grid saves the per-CTA setup that dominates short tiles (Lean
-// P at N = 512 / 1K / 2K: 718 / 947 / 1125 against 461 / 734 / 1047; exact
-// P at 4K: 1345 against 1298), and at d_qk = 192.
+// The FP8 forward's kernel per mode, head dimension and length, by
+// measurement on GB300 (outputs bit-identical between the kernels): the
+// two-tile kernel (fwd3.cuh) at d_qk = 128 for Lean P beyond 2048 keys and
+// exact P beyond 4096 (d128 N = 32K: Lean 1866 against 1609 TFLOP/s for the
+// persistent kernel, exact 1789 against 1667), and at d_qk = 192 for Lean P
+// beyond 4096 keys (MLA N = 32K: 2190 against 2077; 8K: 1806 against 1728);
+// the persistent kernel over causal pairs (fwd4.cuh) everywhere else: short
+// sequences, where the persistent grid saves the per-CTA setup that
+// dominates short tiles (Lean P at N = 512 / 1K / 2K: 718 / 947 / 1125
+// against 461 / 734 / 1047), and exact P at d_qk = 192 (MLA N = 32K: 2135
+// against 2078 for the two-tile kernel).
 int dispatch_fp8(const void* q, const void* k, const void* v, const FwdArgs& a, const Layout4& L,
                  cudaStream_t s, int d_qk) {
-    if (d_qk == 192) return launch4<192>(q, k, v, a, L, s);
-    const int two_tile_above = a.p_mode == ZYFA_P_LEAN ? 2048 : 4096;
+    const bool lean = a.p_mode == ZYFA_P_LEAN;
+    if (d_qk == 192) return lean && a.N > 4096 ? launch3<192>(q, k, v, a, L, s) : launch4<192>(q, k, v, a, L, s);
+    const int two_tile_above = lean ? 2048 : 4096;
     if (a.N > two_tile_above) return launch3<128>(q, k, v, a, L, s);
     return launch4<128>(q, k, v, a, L, s);
 }
