@@ -5,9 +5,10 @@
 // on AMD CDNA4": running maximum with lazy rescaling, Sec. II-B and IV-A;
 // Lean P and exact P, Sec. IV-B1; per-64-key block scaling, Sec. IV-B2;
 // division by the sum of the rounded probabilities, Sec. IV-B3).  One CTA
-// owns query tiles 2p and 2p + 1, both fed by one K/V ring; TMEM per tile
-// holds one 64-key score half, O, L and the scale factors, and P is staged
-// in shared memory for an SS block-scaled PV.  The softmax: each tile has
+// owns query tiles 2p and 2p + 1, both fed by the same K/V blocks (one ring
+// at d_qk = 128, separate K and V rings at 192); TMEM per tile holds one
+// 64-key score half, O, L and the scale factors, and P is staged in shared
+// memory for an SS block-scaled PV.  The softmax: each tile has
 // one warpgroup per 64-key score half.  Half h of block j is read by
 // warpgroup h, which releases the score buffer at once
 // (so the tile's next QK half starts), and the two warpgroups exchange their
@@ -16,12 +17,15 @@
 // codes of its own 64 keys and writes them into its half of P_j.  The half-1
 // warpgroup also writes the scale factors, waits for PV(j-1), rescales O and
 // L, and publishes P_j together with the half-0 warpgroup (p_full counts
-// both).  Each warpgroup writes 64 of the 128 output columns.
+// both).  Each warpgroup writes 64 of the 128 output columns, staged in its
+// tile's P slots and sent with a bulk tensor store.
 //
 // Lean P or exact P (template parameter LEAN).
 //
-// Warps 0-15 are softmax (warpgroup w: tile w >> 1, half w & 1); warps 16 /
-// 17 issue QK for tiles A / B, 18 / 19 PV (18 also issues the TMA loads).
+// Warps 0-15 are softmax (warpgroup w: tile w >> 1, half w & 1; warp 0 also
+// initialises the barriers and requests Q and the first K/V blocks); warps
+// 16 / 17 issue QK for tiles A / B, 18 / 19 PV (18 also issues the other
+// TMA loads).
 // 640 threads with 96 registers each (one CTA per SM): a softmax thread holds
 // 64 scores.
 #pragma once
