@@ -29,7 +29,10 @@
 //   warps 8-11  correction: rescale O and L in TMEM when a row's maximum
 //               moved (off the softmax's path: the PV of the block waits for
 //               it, the softmax does not; both arrive on the block's p_full),
-//               and the epilogue of each tile (O / L -> BF16 rows, LSE).
+//               and the epilogue of each tile (O / L -> BF16 rows, LSE).  At
+//               d_qk = 128 O leaves through shared memory and bulk tensor
+//               stores, and the next tile's first PV may overwrite O as soon as
+//               O has been read out of TMEM, before the second half is stored.
 //   warp 12     TMA: Q tiles into two slots, K/V blocks into a ring.
 //   warp 13     TMEM owner and QK issuer: QK of block g + 2 is issued as
 //               soon as the scores of block g have been read.
@@ -431,7 +434,17 @@ zyfa_fwd4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             auto lse_at = [&](const TileIter& t) -> size_t {
                 return (static_cast<size_t>(t.b) * args.Hq + t.h) * args.N + static_cast<size_t>(t.qt) * C::BM + row;
             };
-            // O / L of the tile whose last PV arrived on tile_done phase `idx`
+            auto cvt8 = [&](const uint32_t* r, float inv) -> uint4 {
+                uint4 v4;
+                v4.x = cvt_bf16x2(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv);
+                v4.y = cvt_bf16x2(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv);
+                v4.z = cvt_bf16x2(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv);
+                v4.w = cvt_bf16x2(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
+                return v4;
+            };
+            // O / L of the tile whose last PV arrived on tile_done phase `idx`,
+            // written row by row (d_qk = 192: the K/V ring leaves no room for
+            // staging)
             auto epilogue = [&](const TileIter& t, float m_fin, int idx) -> bool {
                 if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::B_TD), idx & 1, abort_flag, 50))) return false;
                 tc_fence_after();
@@ -443,53 +456,75 @@ zyfa_fwd4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // LSE of the rounded weights: l is relative to the final running
                 // max and carries the 2^sigma shift (Sec. IV-B3)
                 if (args.lse) args.lse[lse_at(t)] = logf(l) + (m_fin - kSigma) * 0.6931471805599453f;
-                auto cvt8 = [&](const uint32_t* r) -> uint4 {
-                    uint4 v4;
-                    v4.x = cvt_bf16x2(__uint_as_float(r[0]) * inv, __uint_as_float(r[1]) * inv);
-                    v4.y = cvt_bf16x2(__uint_as_float(r[2]) * inv, __uint_as_float(r[3]) * inv);
-                    v4.z = cvt_bf16x2(__uint_as_float(r[4]) * inv, __uint_as_float(r[5]) * inv);
-                    v4.w = cvt_bf16x2(__uint_as_float(r[6]) * inv, __uint_as_float(r[7]) * inv);
-                    return v4;
-                };
-                if constexpr (C::OST) {
-                    // each 64-column half: the warp's 32 rows into its staging
-                    // (16-byte chunk j of row r at position j ^ (r & 7)), then one
-                    // bulk tensor store; the warp goes on without waiting for it
-                    uint8_t* stg = smem + C::OFF_OST + q4 * C::OST_WARP + lane * 128;
-                    #pragma unroll 1
-                    for (int hf = 0; hf < 2; ++hf) {
-                        // the staging's previous store has read it
-                        if (lane == 0) bulk_wait_read();
-                        __syncwarp();
-                        #pragma unroll 1
-                        for (int c = 0; c < 2; ++c) {
-                            uint32_t r[32];
-                            tmem_ld32(t_row + C::COL_O + hf * 64 + c * 32, r);
-                            tmem_wait_ld();
-                            #pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                *reinterpret_cast<uint4*>(stg + (((4 * c + k) ^ (lane & 7)) << 4)) = cvt8(r + 8 * k);
-                        }
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                        __syncwarp();
-                        if (lane == 0) {
-                            tma_store_4d(&tm_o, smem_u32(smem + C::OFF_OST + q4 * C::OST_WARP), 64 * hf, t.h,
-                                         t.qt * C::BM + 32 * q4, t.b);
-                            bulk_commit();
-                        }
-                    }
-                } else {
-                    uint4* dst = out_row(t);
-                    #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(t_row + C::COL_O + c * 32, r);
-                        tmem_wait_ld();
-                        #pragma unroll
-                        for (int k = 0; k < 4; ++k) dst[c * 4 + k] = cvt8(r + 8 * k);
-                    }
+                uint4* dst = out_row(t);
+                #pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(t_row + C::COL_O + c * 32, r);
+                    tmem_wait_ld();
+                    #pragma unroll
+                    for (int k = 0; k < 4; ++k) dst[c * 4 + k] = cvt8(r + 8 * k, inv);
                 }
                 return true;
+            };
+            // d_qk = 128: the epilogue in two steps around the arrival that lets
+            // the next tile's first PV overwrite O.  epi_read waits for the
+            // tile's last PV (tile_done phase `idx`), sends the first 64 columns
+            // of O / L on their way and converts the last 64 into `hold`, so that
+            // nothing of the tile is left in TMEM; epi_write sends `hold` and the
+            // LSE once that arrival is made.  Each 64-column half goes through
+            // the warp's staging (16-byte chunk j of row r at position j ^ (r &
+            // 7)), once the previous store has read it, and leaves in one bulk
+            // tensor store that the warp does not wait for.
+            uint4 hold[8];
+            float l_fin = 1.0f;
+            uint8_t* stg = smem + C::OFF_OST + q4 * C::OST_WARP + lane * 128;
+            auto stage_out = [&](const TileIter& t, int col) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_4d(&tm_o, smem_u32(smem + C::OFF_OST + q4 * C::OST_WARP), col, t.h,
+                                 t.qt * C::BM + 32 * q4, t.b);
+                    bulk_commit();
+                }
+            };
+            auto epi_read = [&](const TileIter& t, int idx) -> bool {
+                if (!__all_sync(0xffffffffu, mbar_wait(BAR(C::B_TD), idx & 1, abort_flag, 50))) return false;
+                tc_fence_after();
+                uint32_t lr;
+                tmem_ld1(t_row + C::COL_L, lr);
+                tmem_wait_ld();
+                l_fin = __uint_as_float(lr);
+                const float inv = dv / l_fin;
+                if (lane == 0) bulk_wait_read();
+                __syncwarp();
+                #pragma unroll 1
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(t_row + C::COL_O + c * 32, r);
+                    tmem_wait_ld();
+                    #pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        *reinterpret_cast<uint4*>(stg + (((4 * c + k) ^ (lane & 7)) << 4)) = cvt8(r + 8 * k, inv);
+                }
+                stage_out(t, 0);
+                #pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(t_row + C::COL_O + 64 + c * 32, r);
+                    tmem_wait_ld();
+                    #pragma unroll
+                    for (int k = 0; k < 4; ++k) hold[4 * c + k] = cvt8(r + 8 * k, inv);
+                }
+                return true;
+            };
+            auto epi_write = [&](const TileIter& t, float m_fin) {
+                if (lane == 0) bulk_wait_read();
+                __syncwarp();
+                #pragma unroll
+                for (int e = 0; e < 8; ++e) *reinterpret_cast<uint4*>(stg + ((e ^ (lane & 7)) << 4)) = hold[e];
+                stage_out(t, 64);
+                if (args.lse) args.lse[lse_at(t)] = logf(l_fin) + (m_fin - kSigma) * 0.6931471805599453f;
             };
             bool ok = true;
             bool pend = false;          // a tile whose epilogue is still due
@@ -509,10 +544,15 @@ zyfa_fwd4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 for (int j = 0; j < t.nb; ++j, ++gc) {
                     const int sl = gc % C::NSLOT;
-                    if (j == 0 && pend) {
+                    const bool flush = j == 0 && pend;
+                    if (flush) {
                         // the previous tile's O leaves TMEM before PV(g) overwrites it
-                        if (!(ok = epilogue(pt, pm, tq - 1))) break;
-                        pend = false;
+                        if constexpr (C::OST) {
+                            if (!(ok = epi_read(pt, tq - 1))) break;
+                        } else {
+                            if (!(ok = epilogue(pt, pm, tq - 1))) break;
+                            pend = false;
+                        }
                     }
                     if (!(ok = __all_sync(0xffffffffu, mbar_wait(BAR(C::B_FR + 4 * sl + q4), (gc / C::NSLOT) & 1,
                                                                    abort_flag, 51))))
@@ -543,6 +583,10 @@ zyfa_fwd4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                     tc_fence_before();
                     mbar_arrive(BAR(C::B_PF + sl));
+                    if (C::OST && flush) {
+                        epi_write(pt, pm);
+                        pend = false;
+                    }
                     if (j == t.nb - 1) {
                         pend = true;
                         pt = t;
@@ -551,7 +595,13 @@ zyfa_fwd4_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 ++tq;
             }
-            if (ok && pend) ok = epilogue(pt, pm, tq - 1);
+            if (ok && pend) {
+                if constexpr (C::OST) {
+                    if ((ok = epi_read(pt, tq - 1))) epi_write(pt, pm);
+                } else {
+                    ok = epilogue(pt, pm, tq - 1);
+                }
+            }
             // the output's bulk stores complete before the CTA exits
             if (C::OST && lane == 0) bulk_wait_all();
             __syncwarp();
