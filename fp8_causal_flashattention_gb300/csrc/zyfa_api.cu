@@ -200,17 +200,18 @@ int launch(const void* q, const void* k, const void* v, const FwdArgs& a, const 
 // measurement on GB300 (outputs bit-identical between the kernels): the
 // two-tile kernel (fwd3.cuh) at d_qk = 128 for Lean P beyond 2048 keys and
 // exact P beyond 4096 (d128 N = 32K: Lean 1866 against 1609 TFLOP/s for the
-// persistent kernel, exact 1789 against 1667), and at d_qk = 192 for Lean P
-// beyond 4096 keys (MLA N = 32K: 2190 against 2077; 8K: 1806 against 1728);
-// the persistent kernel over causal pairs (fwd4.cuh) everywhere else: short
+// persistent kernel, exact 1789 against 1667; N = 4K exact 1298 against
+// 1449), and at d_qk = 192 for Lean P beyond 16384 keys (MLA N = 32K: 2201
+// against 2118; 16K: 2058 against 2101, 8K: 1822 against 1879); the
+// persistent kernel over causal pairs (fwd4.cuh) everywhere else: short
 // sequences, where the persistent grid saves the per-CTA setup that
-// dominates short tiles (Lean P at N = 512 / 1K / 2K: 718 / 947 / 1125
+// dominates short tiles (Lean P at N = 512 / 1K / 2K: 815 / 1090 / 1226
 // against 461 / 734 / 1047), and exact P at d_qk = 192 (MLA N = 32K: 2135
 // against 2078 for the two-tile kernel).
 int dispatch_fp8(const void* q, const void* k, const void* v, const FwdArgs& a, const Layout4& L,
                  cudaStream_t s, int d_qk) {
     const bool lean = a.p_mode == ZYFA_P_LEAN;
-    if (d_qk == 192) return lean && a.N > 4096 ? launch3<192>(q, k, v, a, L, s) : launch4<192>(q, k, v, a, L, s);
+    if (d_qk == 192) return lean && a.N > 16384 ? launch3<192>(q, k, v, a, L, s) : launch4<192>(q, k, v, a, L, s);
     const int two_tile_above = lean ? 2048 : 4096;
     if (a.N > two_tile_above) return launch3<128>(q, k, v, a, L, s);
     return launch4<128>(q, k, v, a, L, s);
