@@ -62,6 +62,25 @@ def test_all_rows_and_lse(lib, kind, mode):
     assert err.max() <= 2e-2 and np.sqrt(np.mean(err ** 2)) <= 5e-4, (err.max(), np.sqrt(np.mean(err ** 2)))
 
 
+@pytest.mark.parametrize("mode", ["lean", "exact"])
+def test_odd_tile_count_all_rows(lib, mode):
+    """An odd number of query tiles just above each mode's switch to this
+    kernel (Lean P 17 tiles, exact P 33): the last CTA holds one tile and
+    releases every K/V stage it reads alone; every row against the oracle,
+    with the LSE."""
+    Z = lib
+    N = (2048 if mode == "lean" else 4096) + 128
+    wl, inp, ((q, k, v), ds) = _setup("gaussian", Hq=2, Hkv=1, seed=27, N=N)
+    out, lse = Z.attention_fp8(q, k, v, ds[0], ds[1], ds[2], return_lse=True, **_mode_args(Z, mode))
+    rows = np.arange(wl.B * wl.Hq * wl.N)
+    res = P.errors(P.gather_rows(out, wl, rows), inp, mode, rows, extra=False)
+    print(mode, res)
+    assert P.passes(res, mode) and res["rel_l2"] <= STRICT_REL_L2, res
+    _, _, ref_lse = oracle.fwd(P.oracle_params(wl, inp, mode), inp.q8, inp.k8, inp.v8, rows)
+    err = np.abs(_lse_rows(lse) - ref_lse)
+    assert err.max() <= 2e-2 and np.sqrt(np.mean(err ** 2)) <= 5e-4
+
+
 @pytest.mark.parametrize("kind", ["gaussian", "sink"])
 def test_mla_lean_rows(lib, kind):
     """Lean P at d_qk = 192 beyond 16384 keys: the two-tile kernel with separate
