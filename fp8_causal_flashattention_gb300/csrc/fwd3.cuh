@@ -73,18 +73,28 @@ struct Fwd3Cfg {
     static constexpr int OFF_BAR = OFF_ONES + ONES_BYTES;
     // q_full, k_full[NSK], v_full[NSV], k_empty[NSK] (one ring: the stage's
     // empty barrier), v_empty[NSV] (split rings only), s_full[2][2],
-    // s_free[2], p_full[2], o_done[2], fin[2], mma_done[4], exchange[2]; then
-    // the TMEM slot and the abort flag
-    static constexpr int NBAR = 1 + NSK + NSV + NSK + (SPLIT ? NSV : 0) + 18;
+    // s_free[2], p_full[2], o_done[2], fin[2], mma_done[4], exchange[2],
+    // q_tmem[2]; then the TMEM slot and the abort flag
+    static constexpr int NBAR = 1 + NSK + NSV + NSK + (SPLIT ? NSV : 0) + 20;
     static constexpr int SMEM_BYTES = OFF_BAR + NBAR * 8 + 16;
     static constexpr int SMEM_ALLOC = SMEM_BYTES;
+    // d_qk = 128: Q in TMEM (32 columns per tile), the A operand of QK, so
+    // that a QK half reads only K from shared memory (an SS MMA with N = 64
+    // is bound by its shared-memory operands); at 192 Q (48 columns a tile)
+    // does not fit and QK reads it from shared memory
+    static constexpr bool QT = DQK == 128;
     static __host__ __device__ constexpr uint32_t col_s(int t) { return 64u * t; }
     static __host__ __device__ constexpr uint32_t col_o(int t) { return 128u + 128u * t; }
-    static __host__ __device__ constexpr uint32_t col_l(int t) { return 384u + 16u * t; }
-    static __host__ __device__ constexpr uint32_t col_sfa(int t, int slot) { return 416u + 16u * t + 4u * slot; }
-    static __host__ __device__ constexpr uint32_t col_sfb(int t) { return 424u + 16u * t; }
+    static __host__ __device__ constexpr uint32_t col_q(int t) { return 384u + 32u * t; }
+    static __host__ __device__ constexpr uint32_t col_l(int t) { return (QT ? 448u : 384u) + 16u * t; }
+    static __host__ __device__ constexpr uint32_t col_sfa(int t, int slot) {
+        return QT ? 480u + 8u * t + 4u * slot : 416u + 16u * t + 4u * slot;
+    }
+    static __host__ __device__ constexpr uint32_t col_sfb(int t) { return QT ? 496u + 4u * t : 424u + 16u * t; }
     // half maxima exchanged between a tile's two warpgroups, by block parity
-    static __host__ __device__ constexpr uint32_t col_x(int t, int hf, int par) { return 448u + 4u * t + 2u * hf + par; }
+    static __host__ __device__ constexpr uint32_t col_x(int t, int hf, int par) {
+        return (QT ? 504u : 448u) + 4u * t + 2u * hf + par;
+    }
     static constexpr uint32_t TMEM_COLS = 512;
 };
 
@@ -113,6 +123,7 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int B_SX = B_SF + 4, B_PF = B_SX + 2, B_OD = B_PF + 2;
     const int B_FIN = B_OD + 2, B_MD = B_FIN + 2;   // B_MD: [4], one per issuer warp
     const int B_X = B_MD + 4;                        // [2]: a tile's half maxima exchanged
+    const int B_QT = B_X + 2;                        // [2]: a tile's Q copied into TMEM
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + C::NBAR * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -165,7 +176,7 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         for (int i = lane; i < C::NBAR; i += 32) {
             uint32_t n = 1;                           // q_full, k_full, v_full, s_full, o_done, fin, mma_done
             if (i >= B_KE && i < B_SF) n = 2;     // one commit per QK (split K) or PV issuer
-            else if (i == B_SX || i == B_SX + 1) n = 128;
+            else if (i == B_SX || i == B_SX + 1 || i == B_QT || i == B_QT + 1) n = 128;
             else if (i == B_PF || i == B_PF + 1 || i == B_X || i == B_X + 1) n = 256;   // both warpgroups of the tile
             mbar_init(BAR(i), n);
         }
@@ -228,14 +239,20 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int kk = 0; kk < C::QK_STEPS; ++kk) {
                 const int off = kk * 32;
                 const int ch = off / C::CB, in = off % C::CB;
-                mma_ss_elect<1>(tmem + C::col_s(t),
-                                dq + static_cast<uint64_t>((ch * (C::BM * C::CB) + in) >> 4),
-                                dk + static_cast<uint64_t>((ch * (C::BN * C::CB) + in) >> 4), kQK,
-                                kk > 0 ? 1u : 0u);
+                if constexpr (C::QT)
+                    // 32 bytes of Q per K step = 8 TMEM columns
+                    mma_ts_f8_elect(tmem + C::col_s(t), tmem + C::col_q(t) + 8u * kk,
+                                    dk + static_cast<uint64_t>((ch * (C::BN * C::CB) + in) >> 4), kQK,
+                                    kk > 0 ? 1u : 0u);
+                else
+                    mma_ss_elect<1>(tmem + C::col_s(t),
+                                    dq + static_cast<uint64_t>((ch * (C::BM * C::CB) + in) >> 4),
+                                    dk + static_cast<uint64_t>((ch * (C::BN * C::CB) + in) >> 4), kQK,
+                                    kk > 0 ? 1u : 0u);
             }
             tc_commit_elect(BAR(B_SF + 2 * t + hf));
         };
-        bool ok = nbt > 0 && wait_warp(B_QF, 0, 22);
+        bool ok = nbt > 0 && wait_warp(C::QT ? B_QT + t : B_QF, 0, 22);
         for (int j = 0; ok && j < nbt; ++j) {
             if (j > 0 && !(ok = wait_warp(B_SX + t, 1, 31))) break;       // half 1 of j-1 read
             if (!(ok = wait_warp(B_KF + j % C::NSK, (j / C::NSK) & 1, 27))) break;
@@ -398,6 +415,30 @@ zyfa_fwd3_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tmem_st4(t_row + C::col_sfb(t), 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
         float m_run = -INFINITY;                              // running max (base 2)
         bool ok = true;
+        if constexpr (C::QT) {
+            // the half-0 warpgroup copies its tile's Q rows into TMEM once:
+            // 16-byte chunk c of row r sits at chunk c ^ (r & 7) of the row's
+            // 128 bytes in the TMA-loaded tile (128-byte swizzle)
+            if (hf == 0 && nbt > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(BAR(B_QF), 0, abort_flag, 35));
+                if (ok) {
+                    const uint8_t* qrow = smem + C::OFF_Q + t * C::Q_BYTES + row * 128;
+                    uint32_t qw[32];
+                    #pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(qrow + ((c ^ (row & 7)) << 4));
+                        qw[4 * c + 0] = v.x;
+                        qw[4 * c + 1] = v.y;
+                        qw[4 * c + 2] = v.z;
+                        qw[4 * c + 3] = v.w;
+                    }
+                    tmem_st32(t_row + C::col_q(t), qw);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(BAR(B_QT + t));
+                }
+            }
+        }
 
         // e4m3 codes of 16 scores relative to maximum m with block exponent o
         const uint64_t k256 = pack2f(256.0f, 256.0f);

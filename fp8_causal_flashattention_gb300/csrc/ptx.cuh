@@ -337,6 +337,16 @@ __device__ __forceinline__ void mma_ts_f16_elect(uint32_t d, uint32_t a_tmem, ui
                  :: "r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
 }
 
+// D(tmem) (+)= A(tmem) * B(smem)^T, kind::f8f6f4 (A: one row per TMEM lane,
+// 4 bytes of K per column).
+__device__ __forceinline__ void mma_ts_f8_elect(uint32_t d, uint32_t a_tmem, uint64_t b,
+                                                uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p, e;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "elect.sync _|e, 0xffffffff;\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}"
+                 :: "r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
 __device__ __forceinline__ void mma_ts_mx8_elect(uint32_t d, uint32_t a_tmem, uint64_t b,
                                                  uint32_t idesc, uint32_t sfa, uint32_t sfb,
                                                  uint32_t acc) {
