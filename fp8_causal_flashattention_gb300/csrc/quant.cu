@@ -333,9 +333,14 @@ __global__ void __launch_bounds__(kThreads) pass_kernel(const QuantArgs a) {
     }
     const uint32_t lane_h = (blockIdx.x * kRowsPerIter + sub) % a.H;
     uint32_t batch_end = 0;                   // first row past the cached mean's batch
-    // one line of E + 4 floats per thread: (E + 4) / 4 is odd, so the 8
-    // lanes of a quarter warp read 16-byte pieces in 8 distinct bank groups
-    __shared__ __align__(16) float mu_s[SMOOTH ? kThreads : 1][SMOOTH ? E + 4 : 4];
+    // The lane's slice of the mean: in registers at D = 128 (32 floats);
+    // at D = 192 in one shared-memory line of E + 4 floats per thread ((E +
+    // 4) / 4 is odd, so the 8 lanes of a quarter warp read 16-byte pieces in
+    // 8 distinct bank groups)
+    constexpr bool MU_REG = SMOOTH && D == 128;
+    constexpr bool MU_SMEM = SMOOTH && !MU_REG;
+    __shared__ __align__(16) float mu_s[MU_SMEM ? kThreads : 1][MU_SMEM ? E + 4 : 4];
+    float mu_r[MU_REG ? E : 1];
     uint4 raw[NC];
     uint32_t g = blockIdx.x;
     if (g < steps) load_raw<D, ROT>(a.x + static_cast<size_t>(min(g * kRowsPerIter + sub, total - 1)) * D,
@@ -362,9 +367,10 @@ __global__ void __launch_bounds__(kThreads) pass_kernel(const QuantArgs a) {
             // the lane's head is fixed (grid * 64 is a multiple of H); its
             // mean, with the signs of diag(s) applied (s(x - mean) equals
             // s x - s mean exactly), is reloaded when the batch changes.  It
-            // sits in the thread's own shared-memory line; each lane reads
-            // back only the values it wrote itself, so no barrier is needed.
-            float4* mine = reinterpret_cast<float4*>(&mu_s[threadIdx.x][0]);
+            // sits in registers or the thread's own shared-memory line; each
+            // lane reads back only the values it wrote itself, so no barrier
+            // is needed.
+            float4* mine = reinterpret_cast<float4*>(&mu_s[MU_SMEM ? threadIdx.x : 0][0]);
             if (r >= batch_end) {
                 const uint32_t b = r / a.NH;
                 batch_end = (b + 1) * a.NH;
@@ -384,14 +390,26 @@ __global__ void __launch_bounds__(kThreads) pass_kernel(const QuantArgs a) {
                             f.z = __uint_as_float(__float_as_uint(f.z) ^ (w1 << 16));
                             f.w = __uint_as_float(__float_as_uint(f.w) ^ (w1 & 0x80000000u));
                         }
-                        mine[c * 2 + k] = f;
+                        if constexpr (MU_REG) {
+                            mu_r[c * 8 + 4 * k + 0] = f.x;
+                            mu_r[c * 8 + 4 * k + 1] = f.y;
+                            mu_r[c * 8 + 4 * k + 2] = f.z;
+                            mu_r[c * 8 + 4 * k + 3] = f.w;
+                        } else {
+                            mine[c * 2 + k] = f;
+                        }
                     }
             }
 #pragma unroll
             for (int c = 0; c < NC; ++c)
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
-                    const float4 f = mine[c * 2 + k];
+                    float4 f;
+                    if constexpr (MU_REG)
+                        f = make_float4(mu_r[c * 8 + 4 * k + 0], mu_r[c * 8 + 4 * k + 1],
+                                        mu_r[c * 8 + 4 * k + 2], mu_r[c * 8 + 4 * k + 3]);
+                    else
+                        f = mine[c * 2 + k];
                     sub2(v[c * 8 + 4 * k + 0], v[c * 8 + 4 * k + 1], f.x, f.y);
                     sub2(v[c * 8 + 4 * k + 2], v[c * 8 + 4 * k + 3], f.z, f.w);
                 }
